@@ -1,0 +1,402 @@
+// fa_api.cu -- the C ABI of libfa_gb300.so (declared in include/fa.h):
+// argument validation, device checks, TMA descriptor encoding, workspace
+// handling and dispatch to the prefill or decode kernels.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_internal.h"
+#include "fa_launch.h"
+
+namespace fa {
+
+int prefill_smem_bytes_d128();
+int prefill_smem_bytes_d64();
+cudaError_t prefill_num_regs_d128(bool bf16, int* regs);
+cudaError_t prefill_num_regs_d64(bool bf16, int* regs);
+cudaError_t launch_prefill_d128(bool, const CUtensorMap&, const CUtensorMap&,
+                                const CUtensorMap&, const CUtensorMap&,
+                                const PrefillParams&, int, cudaStream_t);
+cudaError_t launch_prefill_d64(bool, const CUtensorMap&, const CUtensorMap&,
+                               const CUtensorMap&, const CUtensorMap&,
+                               const PrefillParams&, int, cudaStream_t);
+
+int prefill_smem_bytes(int D) {
+  return D == 128 ? prefill_smem_bytes_d128() : prefill_smem_bytes_d64();
+}
+cudaError_t prefill_num_regs(int D, bool bf16, int* regs) {
+  return D == 128 ? prefill_num_regs_d128(bf16, regs)
+                  : prefill_num_regs_d64(bf16, regs);
+}
+cudaError_t launch_prefill(int D, bool bf16, const CUtensorMap& q,
+                           const CUtensorMap& k, const CUtensorMap& v,
+                           const CUtensorMap& o, const PrefillParams& p,
+                           int grid, cudaStream_t stream) {
+  return D == 128 ? launch_prefill_d128(bf16, q, k, v, o, p, grid, stream)
+                  : launch_prefill_d64(bf16, q, k, v, o, p, grid, stream);
+}
+
+}  // namespace fa
+
+namespace {
+
+// Device status word: kernels record FA_ERR_TIMEOUT here.
+__device__ unsigned g_status_word;
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kDefaultWatchdogNs = 1000000000ull;
+std::atomic<unsigned long long> g_watchdog_ns{kDefaultWatchdogNs};
+
+struct DeviceState {
+  bool probed = false;
+  fa_status_t usable = FA_ERR_UNSUPPORTED;
+  int sm_count = 0;
+  unsigned* status = nullptr;
+  bool regs_ok[2][2] = {};  // [D==128][bf16]
+  bool regs_checked[2][2] = {};
+  void* workspace = nullptr;  // fa_fwd's cached decode workspace
+  size_t workspace_bytes = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+fa_status_t get_encoder() {
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode ? FA_OK : FA_ERR_CUDA;
+}
+
+// Current device's state; checks compute capability 10.3 once.
+fa_status_t current_device(DeviceState** out, int* dev_out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& d = g_dev[dev];
+  if (!d.probed) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return FA_ERR_CUDA;
+    d.probed = true;
+    d.sm_count = sms;
+    if (major != 10 || minor != 3) {
+      d.usable = FA_ERR_UNSUPPORTED;
+    } else {
+      void* addr = nullptr;
+      if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) {
+        d.probed = false;
+        return FA_ERR_CUDA;
+      }
+      d.status = static_cast<unsigned*>(addr);
+      d.usable = FA_OK;
+    }
+  }
+  if (d.usable != FA_OK) return d.usable;
+  *out = &d;
+  if (dev_out) *dev_out = dev;
+  return FA_OK;
+}
+
+bool aligned16(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+fa_status_t validate(const void* q, const void* k, const void* v, const void* o,
+                     const void* lse, int B, int H, int Sq, int Skv, int D,
+                     float scale, int dtype) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      !aligned16(lse))
+    return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || Sq < 1 || Skv < 1) return FA_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H >= 65536) return FA_ERR_INVALID_ARG;
+  if (Sq > (1 << 24) || Skv > (1 << 24)) return FA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  if (dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+// 3-D view [B*H, S, D] of a [B,H,S,D] tensor; boxes of 64 columns x rows.
+fa_status_t encode_3d(CUtensorMap* m, const void* base, int D, int S, int BH,
+                      int box_rows, bool bf16) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                                 static_cast<cuuint64_t>(S) * D * 2};
+  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), 1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUresult r = g_encode(
+      m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+      const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status_t run_prefill(DeviceState& d, const void* q, const void* k, const void* v,
+                        void* o, float* lse, int B, int H, int Sq, int Skv, int D,
+                        float scale, int causal, bool bf16, unsigned flags,
+                        cudaStream_t stream) {
+  fa_status_t st = get_encoder();
+  if (st != FA_OK) return st;
+  {
+    const int di = D == 128 ? 1 : 0, ti = bf16 ? 1 : 0;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!d.regs_checked[di][ti]) {
+      // the register split inside the kernel assumes 128 registers/thread
+      int regs = 0;
+      if (fa::prefill_num_regs(D, bf16, &regs) != cudaSuccess) return FA_ERR_CUDA;
+      d.regs_checked[di][ti] = true;
+      d.regs_ok[di][ti] = regs == 128;
+    }
+    if (!d.regs_ok[di][ti]) return FA_ERR_UNSUPPORTED;
+  }
+  const int BH = B * H;
+  CUtensorMap tq, tk, tv, to;
+  if ((st = encode_3d(&tq, q, D, Sq, BH, fa::kBM, bf16)) != FA_OK) return st;
+  if ((st = encode_3d(&tk, k, D, Skv, BH, fa::kBN, bf16)) != FA_OK) return st;
+  if ((st = encode_3d(&tv, v, D, Skv, BH, fa::kBN, bf16)) != FA_OK) return st;
+  if ((st = encode_3d(&to, o, D, Sq, BH, 32, bf16)) != FA_OK) return st;
+  fa::PrefillParams p{};
+  p.lse = lse;
+  p.status = d.status;
+  p.timeout_ns = g_watchdog_ns.load();
+  p.BH = BH;
+  p.Sq = Sq;
+  p.Skv = Skv;
+  p.n_qtiles = (Sq + fa::kRowsPerCta - 1) / fa::kRowsPerCta;
+  p.causal = causal ? 1 : 0;
+  p.lpt = (flags & FA_FLAG_NO_LPT) ? 0 : 1;
+  p.always_rescale = (flags & FA_FLAG_ALWAYS_RESCALE) ? 1 : 0;
+  p.test_stall = (flags & FA_FLAG_TEST_STALL) ? 1 : 0;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  const long long grid = static_cast<long long>(p.n_qtiles) * BH;
+  if (grid > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  if (fa::launch_prefill(D, bf16, tq, tk, tv, to, p, static_cast<int>(grid), stream) !=
+      cudaSuccess)
+    return FA_ERR_CUDA;
+  return FA_OK;
+}
+
+// Key split for decode: enough CTAs for many waves over two CTAs per SM,
+// at least 256 keys per split, a multiple of the 64-key tile.
+int decode_keys_per_split(int BH, int Skv, int sm_count, int num_splits) {
+  const int tile = fa::kDecKeysPerTile;
+  if (num_splits >= 1) {
+    int kps = (Skv + num_splits - 1) / num_splits;
+    return ((kps + tile - 1) / tile) * tile;
+  }
+  const long long slots = 2LL * (sm_count > 0 ? sm_count : 148);
+  long long kps = (static_cast<long long>(BH) * Skv + 16 * slots - 1) / (16 * slots);
+  kps = ((kps + tile - 1) / tile) * tile;
+  if (kps < 256) kps = 256;
+  if (kps > 2048) kps = 2048;
+  const long long skv_r = ((static_cast<long long>(Skv) + tile - 1) / tile) * tile;
+  if (kps > skv_r) kps = skv_r;
+  return static_cast<int>(kps);
+}
+
+size_t decode_ws_bytes(int BH, int n_splits, int D) {
+  if (n_splits <= 1) return 0;
+  const size_t po = static_cast<size_t>(n_splits) * BH * D * sizeof(float);
+  const size_t pl = static_cast<size_t>(n_splits) * BH * sizeof(float);
+  return ((po + 255) / 256) * 256 + ((pl + 255) / 256) * 256;
+}
+
+fa_status_t run_decode(DeviceState& d, const void* q, const void* k, const void* v,
+                       void* o, float* lse, int BH, int Skv, int D, float scale,
+                       bool bf16, int num_splits, void* ws, size_t ws_bytes,
+                       bool own_ws, cudaStream_t stream) {
+  const int kps = decode_keys_per_split(BH, Skv, d.sm_count, num_splits);
+  const int n_splits = (Skv + kps - 1) / kps;
+  const size_t need = decode_ws_bytes(BH, n_splits, D);
+  if (need > 0) {
+    if (own_ws) {
+      std::lock_guard<std::mutex> lock(g_mu);
+      if (d.workspace_bytes < need) {
+        if (d.workspace) cudaFree(d.workspace);
+        d.workspace = nullptr;
+        d.workspace_bytes = 0;
+        if (cudaMalloc(&d.workspace, need) != cudaSuccess) return FA_ERR_CUDA;
+        d.workspace_bytes = need;
+      }
+      ws = d.workspace;
+    } else {
+      if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u))
+        return FA_ERR_WORKSPACE;
+    }
+  }
+  fa::DecodeParams p{};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.o = o;
+  p.lse = lse;
+  if (need > 0) {
+    const size_t po = static_cast<size_t>(n_splits) * BH * D * sizeof(float);
+    p.part_o = static_cast<float*>(ws);
+    p.part_lse = reinterpret_cast<float*>(static_cast<char*>(ws) + ((po + 255) / 256) * 256);
+  }
+  p.status = d.status;
+  p.timeout_ns = g_watchdog_ns.load();
+  p.BH = BH;
+  p.Skv = Skv;
+  p.n_splits = n_splits;
+  p.keys_per_split = kps;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  const long long grid = static_cast<long long>(BH) * n_splits;
+  if (grid > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  if (fa::launch_decode(D, bf16, p, static_cast<int>(grid), stream) != cudaSuccess)
+    return FA_ERR_CUDA;
+  if (n_splits > 1 && fa::launch_decode_combine(D, bf16, p, stream) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return FA_OK;
+}
+
+fa_status_t forward(const void* q, const void* k, const void* v, void* o, float* lse,
+                    int B, int H, int Sq, int Skv, int D, float scale, int causal,
+                    int dtype, unsigned flags, int num_splits, void* ws,
+                    size_t ws_bytes, bool own_ws, cudaStream_t stream) {
+  fa_status_t st = validate(q, k, v, o, lse, B, H, Sq, Skv, D, scale, dtype);
+  if (st != FA_OK) return st;
+  if (num_splits < 0) return FA_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  if ((st = current_device(&d, nullptr)) != FA_OK) return st;
+  const bool bf16 = dtype == FA_BF16;
+  // one query row per head: every key is visible (causal or not), and the
+  // split-KV decode kernel serves it
+  if (Sq == 1 && !(flags & FA_FLAG_TEST_STALL))
+    return run_decode(*d, q, k, v, o, lse, B * H, Skv, D, scale, bf16, num_splits, ws,
+                      ws_bytes, own_ws, stream);
+  return run_prefill(*d, q, k, v, o, lse, B, H, Sq, Skv, D, scale, causal, bf16, flags,
+                     stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                   int B, int H, int Sq, int Skv, int D, float scale, int causal,
+                   int dtype, fa_stream_t stream) {
+  return forward(q, k, v, o, lse, B, H, Sq, Skv, D, scale, causal, dtype, 0u, 0,
+                 nullptr, 0, true, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t fa_workspace_bytes(int B, int H, int Sq, int Skv, int D, int num_splits) {
+  if (B < 1 || H < 1 || Sq != 1 || Skv < 1 || (D != 64 && D != 128) || num_splits < 0)
+    return 0;
+  int sms = 0;
+  if (num_splits == 0) {
+    DeviceState* d = nullptr;
+    if (current_device(&d, nullptr) == FA_OK) sms = d->sm_count;
+  }
+  const int kps = decode_keys_per_split(B * H, Skv, sms, num_splits);
+  return decode_ws_bytes(B * H, (Skv + kps - 1) / kps, D);
+}
+
+fa_status_t fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                      int B, int H, int Sq, int Skv, int D, float scale, int causal,
+                      int dtype, unsigned flags, int num_splits, void* workspace,
+                      size_t workspace_bytes, fa_stream_t stream) {
+  return forward(q, k, v, o, lse, B, H, Sq, Skv, D, scale, causal, dtype, flags,
+                 num_splits, workspace, workspace_bytes, false,
+                 reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t fa_host_staging_bytes(int B, int H, int Sq, int Skv, int D) {
+  if (B < 1 || H < 1 || Sq < 1 || Skv < 1 || (D != 64 && D != 128)) return 0;
+  auto up = [](size_t x) { return ((x + 255) / 256) * 256; };
+  const size_t BH = static_cast<size_t>(B) * H;
+  const size_t qb = up(BH * Sq * D * 2), kb = up(BH * Skv * D * 2);
+  const size_t lb = up(BH * Sq * sizeof(float));
+  return qb + 2 * kb + qb + lb + fa_workspace_bytes(B, H, Sq, Skv, D, 0);
+}
+
+fa_status_t fa_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h,
+                        float* lse_h, int B, int H, int Sq, int Skv, int D, float scale,
+                        int causal, int dtype, void* staging, size_t staging_bytes,
+                        fa_stream_t stream) {
+  fa_status_t st = validate(q_h, k_h, v_h, o_h, lse_h, B, H, Sq, Skv, D, scale, dtype);
+  if (st != FA_OK) return st;
+  const size_t need = fa_host_staging_bytes(B, H, Sq, Skv, D);
+  if (!staging || staging_bytes < need || (reinterpret_cast<uintptr_t>(staging) & 255u))
+    return FA_ERR_WORKSPACE;
+  auto up = [](size_t x) { return ((x + 255) / 256) * 256; };
+  const size_t BH = static_cast<size_t>(B) * H;
+  const size_t qn = BH * Sq * D * 2, kn = BH * Skv * D * 2, ln = BH * Sq * sizeof(float);
+  char* base = static_cast<char*>(staging);
+  char* dq = base;
+  char* dk = dq + up(qn);
+  char* dv = dk + up(kn);
+  char* dO = dv + up(kn);
+  char* dl = dO + up(qn);
+  char* dws = dl + up(ln);
+  const size_t ws_bytes = need - static_cast<size_t>(dws - base);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(dq, q_h, qn, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(dk, k_h, kn, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(dv, v_h, kn, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return FA_ERR_CUDA;
+  st = forward(dq, dk, dv, dO, reinterpret_cast<float*>(dl), B, H, Sq, Skv, D, scale,
+               causal, dtype, 0u, 0, ws_bytes ? dws : nullptr, ws_bytes, false, s);
+  if (st != FA_OK) return st;
+  if (cudaMemcpyAsync(o_h, dO, qn, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaMemcpyAsync(lse_h, dl, ln, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return FA_OK;
+}
+
+fa_status_t fa_get_device_status(fa_stream_t stream) {
+  DeviceState* d = nullptr;
+  fa_status_t st = current_device(&d, nullptr);
+  if (st != FA_OK) return st;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FA_ERR_CUDA;
+  unsigned word = 0;
+  if (cudaMemcpy(&word, d->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return FA_ERR_CUDA;
+  const unsigned zero = 0;
+  if (cudaMemcpy(d->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return word == 0 ? FA_OK : static_cast<fa_status_t>(word);
+}
+
+void fa_set_watchdog_ns(unsigned long long ns) {
+  g_watchdog_ns.store(ns ? ns : kDefaultWatchdogNs);
+}
+
+const char* fa_status_string(fa_status_t status) {
+  switch (status) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported head dim, dtype or device";
+    case FA_ERR_CUDA: return "CUDA runtime error";
+    case FA_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+    case FA_ERR_TIMEOUT: return "kernel wait timed out";
+  }
+  return "unknown status";
+}
+
+int fa_version(void) { return 10000; }
+
+}  // extern "C"

@@ -1,0 +1,56 @@
+// fa_internal.h -- parameter blocks and constants shared by the host code and
+// the kernels of libfa_gb300.so (not part of the public ABI).
+#pragma once
+#include <cstdint>
+
+namespace fa {
+
+// Status values written to the device status word (same numbers as
+// fa_status_t in include/fa.h).
+constexpr unsigned kStatusOk = 0;
+constexpr unsigned kStatusTimeout = 5;
+
+// Prefill tiling: a CTA owns kStages query tiles of kBM rows (two ping-pong
+// stages) and walks the keys in tiles of kBN.
+constexpr int kBM = 128;
+constexpr int kBN = 128;
+constexpr int kStages = 2;
+constexpr int kRowsPerCta = kBM * kStages;
+constexpr int kThreads = 512;  // 4 warpgroups
+
+struct PrefillParams {
+  float* lse;                 // [B*H, Sq]
+  unsigned* status;           // device status word
+  unsigned long long timeout_ns;
+  int BH;                     // B*H
+  int Sq, Skv;
+  int n_qtiles;               // ceil(Sq / kRowsPerCta)
+  int causal;
+  int lpt;                    // heaviest-first CTA order (causal only)
+  int always_rescale;
+  int test_stall;
+  float scale_log2;           // scale * log2(e)
+};
+
+// Decode (Sq == 1) split-KV.
+constexpr int kDecThreads = 256;     // 8 consumer warps
+constexpr int kDecKeysPerTile = 64;  // keys per smem stage
+constexpr int kDecStages = 3;        // smem ring depth (two CTAs per SM)
+
+struct DecodeParams {
+  const void* q;              // [BH, D]
+  const void* k;              // [BH, Skv, D]
+  const void* v;              // [BH, Skv, D]
+  void* o;                    // [BH, D] (when n_splits == 1)
+  float* lse;                 // [BH]    (when n_splits == 1)
+  float* part_o;              // [n_splits, BH, D] fp32 (when n_splits > 1)
+  float* part_lse;            // [n_splits, BH]
+  unsigned* status;
+  unsigned long long timeout_ns;
+  int BH, Skv;
+  int n_splits;
+  int keys_per_split;         // multiple of kDecKeysPerTile
+  float scale_log2;
+};
+
+}  // namespace fa

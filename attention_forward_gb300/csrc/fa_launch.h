@@ -1,0 +1,25 @@
+// fa_launch.h -- host-side launch entry points of the kernels (internal).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fa_internal.h"
+
+namespace fa {
+
+// Dynamic shared memory a prefill CTA needs (bytes).
+int prefill_smem_bytes(int D);
+// Registers per thread the compiled prefill kernel was built with.
+cudaError_t prefill_num_regs(int D, bool bf16, int* regs);
+cudaError_t launch_prefill(int D, bool bf16, const CUtensorMap& q,
+                           const CUtensorMap& k, const CUtensorMap& v,
+                           const CUtensorMap& o, const PrefillParams& p,
+                           int grid, cudaStream_t stream);
+
+int decode_smem_bytes(int D);
+cudaError_t launch_decode(int D, bool bf16, const DecodeParams& p, int grid,
+                          cudaStream_t stream);
+cudaError_t launch_decode_combine(int D, bool bf16, const DecodeParams& p,
+                                  cudaStream_t stream);
+
+}  // namespace fa

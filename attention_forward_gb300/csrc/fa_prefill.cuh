@@ -1,0 +1,582 @@
+// fa_prefill.cuh -- fused attention forward (prefill) kernel for sm_103a.
+//
+// One CTA owns 256 query rows of one (batch, head) as two ping-pong stages of
+// 128 rows (the two-Q-tile ping-pong of the B300 G5 page, V21) and streams
+// the keys in tiles of 128.  Warp roles (16 warps, 512 threads):
+//
+//   warps 0-3   softmax, stage 0   one thread per query row (TMEM lane)
+//   warps 4-7   softmax, stage 1
+//   warps 8-11  correction: rescales O in TMEM when a row max moved
+//   warp  12    tcgen05.mma issuer (one thread) + TMEM allocation
+//   warp  13    TMA producer (one thread): Q once, then K/V tiles
+//   warps 14-15 idle (they complete the fourth warpgroup)
+//
+// Per stage s the tensor memory holds S_s = Q_s K^T (128 fp32 columns) and
+// the output accumulator O_s (D fp32 columns): 2*128 + 2*D <= 512 columns.
+// P goes through shared memory in the tensor core's K-major 128-byte swizzled
+// layout (the smem_P choice of the G5 page), so both GEMMs read operands
+// from shared memory.
+//
+// Issue order of the tensor core, per key tile j:
+//     QK_0(j)  PV_1(j-1)  QK_1(j)  PV_0(j)
+// so that each softmax warpgroup has two GEMMs of the other stage to hide
+// behind (the aim of the ping-pong on the G5 page).  K and V use separate
+// slots of one ring with their own full/empty barriers (the decoupled K/V
+// loads of G5 V26), the score buffer is released as soon as softmax has
+// read it (the separate "score free" barrier of V28), and stage 0's PV does
+// not wait for stage 1 (the PV0 barrier of V30).
+//
+// Softmax works in the log2 domain with the scale folded into one FFMA
+// before ex2 (G5 V33 "log2exp2"; "The FA5090 Optimization Journey" section
+// 2.6): t = s*scale*log2(e), m = running max of t, p = 2^(t - m).
+// The correction warpgroup multiplies O by alpha = 2^(m_old - m_new) only
+// when some row of its warp changed its max (alpha != 1): the identity
+// rescale skip of the FA5090 page section 2.8, with the warp-uniform vote it
+// describes; skipping a multiply by exactly 1 is bitwise neutral.
+//
+// Causal (bottom-right): key tiles past the last row's diagonal are never
+// loaded or computed; only tiles that cross the diagonal (or the ragged end
+// of the keys) are masked (FA5090 page section 2.8, diagonal-only masking;
+// section 2.7 causal block skip).  CTAs are ordered heaviest-first (LPT,
+// section 2.7).
+//
+// Every mbarrier wait is bounded by a watchdog; a wait that runs out sets a
+// shared abort flag and the device status word, every role leaves its loop,
+// in-flight TMA loads and MMAs are drained, TMEM is freed and the CTA exits.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+
+template <int D>
+struct PrefillLayout {
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr int kQBytes = kBM * D * 2;    // one stage of Q
+  static constexpr int kPBytes = kBM * kBN * 2;  // one stage of P
+  static constexpr int kKVBytes = kBN * D * 2;   // one K or V tile
+  static constexpr int kBox = 128 * 64 * 2;      // one TMA box (64 cols)
+  static constexpr int kSlots = D == 128 ? 3 : 8;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffP = kOffQ + kStages * kQBytes;
+  static constexpr int kOffKV = kOffP + kStages * kPBytes;
+  static constexpr int kOffMisc = kOffKV + kSlots * kKVBytes;
+  // mbarrier indices
+  static constexpr int Q_FULL = 0;    // [2]
+  static constexpr int S_FULL = 2;    // [2]
+  static constexpr int S_FREE = 4;    // [2]
+  static constexpr int P_FULL = 6;    // [2]
+  static constexpr int A_READY = 8;   // [2]
+  static constexpr int O_READY = 10;  // [2]
+  static constexpr int O_FIXED = 12;  // [2]
+  static constexpr int DRAIN = 14;
+  static constexpr int KV_FULL = 15;            // [kSlots]
+  static constexpr int KV_EMPTY = 15 + kSlots;  // [kSlots]
+  static constexpr int kNumBars = 15 + 2 * kSlots;
+  static constexpr int kOffBars = kOffMisc;
+  static constexpr int kOffAlpha = kOffBars + ((kNumBars * 8 + 15) / 16) * 16;
+  static constexpr int kOffTmemSlot = kOffAlpha + kStages * kBM * 4;
+  static constexpr int kOffAbort = kOffTmemSlot + 4;
+  static constexpr int kMiscBytes = kOffAbort + 4 - kOffMisc;
+  static constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;  // + align
+  static constexpr int kTmemCols = 512;
+  static constexpr int kTmemO = 256;  // O_s at column 256 + s*D
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+// Register split between warpgroups (setmaxnreg): softmax warpgroups get
+// more, the others give theirs back.  The sum over the 512 threads equals
+// 512 * 128, the registers the CTA is launched with; the host checks the
+// compiled register count before the first launch.
+constexpr int kRegsSoftmax = 192;
+constexpr int kRegsOther = 64;
+static_assert(2 * 128 * kRegsSoftmax + 2 * 128 * kRegsOther == kThreads * 128,
+              "register split must equal the launch allocation");
+
+struct Ctl {
+  volatile uint32_t* abort;
+  unsigned* status;
+  unsigned long long timeout;
+};
+
+__device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, Ctl c) {
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*c.abort) return false;
+    if (globaltimer_ns() - t0 > c.timeout) {
+      *c.abort = 1u;
+      atomicExch(c.status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
+// Bounded wait; false when the watchdog fired (here or in another role).
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity,
+                                         const Ctl& c) {
+  return mbar_try_wait(bar, parity) || wait_slow(bar, parity, c);
+}
+
+// Warp-uniform bounded wait (every lane gets the same answer).
+__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity,
+                                              const Ctl& c) {
+  const bool ok = wait_bar(bar, parity, c);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Wait used while draining after an abort: time-bounded only.
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity,
+                                        unsigned long long timeout) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > timeout) return;
+  }
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a,
+                                             uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a),
+               "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (BF16) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  } else {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+// Number of key tiles a stage whose first query row is `row_first` needs.
+__device__ __forceinline__ int stage_tiles(int row_first, int Sq, int Skv,
+                                           int causal) {
+  const int n_all = (Skv + kBN - 1) / kBN;
+  if (!causal) return n_all;
+  const int last_key = row_first + kBM - 1 + (Skv - Sq);
+  if (last_key < 0) return 0;
+  return min(n_all, last_key / kBN + 1);
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_prefill_kernel(const __grid_constant__ CUtensorMap tmQ,
+                      const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV,
+                      const __grid_constant__ CUtensorMap tmO,
+                      const PrefillParams p) {
+  using L = PrefillLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sQ = sbase + L::kOffQ;
+  const uint32_t sP = sbase + L::kOffP;
+  const uint32_t sKV = sbase + L::kOffKV;
+  const uint32_t bars = sbase + L::kOffBars;
+  float* alpha_smem = reinterpret_cast<float*>(smem + L::kOffAlpha);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffTmemSlot);
+  volatile uint32_t* abort_flag =
+      reinterpret_cast<volatile uint32_t*>(smem + L::kOffAbort);
+  auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- work item (heaviest-first for causal) ----
+  int qtile, bh;
+  if (p.causal && p.lpt) {
+    qtile = p.n_qtiles - 1 - static_cast<int>(blockIdx.x) / p.BH;
+    bh = static_cast<int>(blockIdx.x) % p.BH;
+  } else {
+    qtile = static_cast<int>(blockIdx.x) % p.n_qtiles;
+    bh = static_cast<int>(blockIdx.x) / p.n_qtiles;
+  }
+  const int row0 = qtile * kRowsPerCta;
+  const int nT0 = stage_tiles(row0, p.Sq, p.Skv, p.causal);
+  const int nT1 = stage_tiles(row0 + kBM, p.Sq, p.Skv, p.causal);
+  const int n_kv = nT1;  // nT1 >= nT0
+
+  // ---- setup ----
+  if (threadIdx.x == 0) {
+    mbar_init(bar(L::Q_FULL + 0), 1);
+    mbar_init(bar(L::Q_FULL + 1), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(L::S_FULL + s), 1);
+      mbar_init(bar(L::S_FREE + s), 4);
+      mbar_init(bar(L::P_FULL + s), 4);
+      mbar_init(bar(L::A_READY + s), 4);
+      mbar_init(bar(L::O_READY + s), 1);
+      mbar_init(bar(L::O_FIXED + s), 4);
+    }
+    mbar_init(bar(L::DRAIN), 1);
+    for (int i = 0; i < L::kSlots; ++i) {
+      mbar_init(bar(L::KV_FULL + i), 1);
+      mbar_init(bar(L::KV_EMPTY + i), 1);
+    }
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 12) {
+    tmem_alloc(smem_u32(tmem_slot), L::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 13 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmO);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Ctl ctl{abort_flag, p.status, p.timeout_ns};
+
+  const int wg = warp >> 2;
+  if (wg < 2) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+  } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
+  }
+
+  if (wg < 2) {
+    // =========================== softmax, stage s ===========================
+    const int s = wg;
+    const int rq = warp & 3;                 // lane quarter of TMEM
+    const int r = rq * 32 + lane;            // row within the stage
+    const int stage_row0 = row0 + s * kBM;
+    const int row_g = stage_row0 + r;        // query row
+    const int nT = s == 0 ? nT0 : nT1;
+    const int off = p.Skv - p.Sq;
+    const uint32_t t_lane = static_cast<uint32_t>(rq * 32) << 16;
+    const uint32_t tS = tmem + t_lane + static_cast<uint32_t>(s * kBN);
+    const uint32_t tO = tmem + t_lane + static_cast<uint32_t>(L::kTmemO + s * D);
+    const uint32_t pbuf = sP + static_cast<uint32_t>(s * L::kPBytes);
+    const float c = p.scale_log2;
+    float m = -INFINITY;  // running max of c*s (log2 units)
+    float l = 0.f;        // running sum of 2^(c*s - m)
+    bool ok = true;
+
+#pragma unroll 1
+    for (int j = 0; j < nT; ++j) {
+      if (!wait_bar_warp(bar(L::S_FULL + s), j & 1, ctl)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t sr[8][16];
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) tmem_ld16(tS + cc * 16, sr[cc]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) reg_fence16(sr[cc]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::S_FREE + s));
+
+      // mask: ragged key tail, and the causal diagonal
+      const int key0 = j * kBN;
+      const bool need_mask =
+          (key0 + kBN > p.Skv) || (p.causal && key0 + kBN - 1 > stage_row0 + off);
+      if (need_mask) {
+        int lim = p.Skv - 1 - key0;
+        if (p.causal) lim = min(lim, row_g + off - key0);
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc)
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            if (cc * 16 + e > lim) sr[cc][e] = __float_as_uint(-INFINITY);
+      }
+      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc)
+#pragma unroll
+        for (int e = 0; e < 16; e += 4) {
+          mx0 = fmaxf(mx0, __uint_as_float(sr[cc][e + 0]));
+          mx1 = fmaxf(mx1, __uint_as_float(sr[cc][e + 1]));
+          mx2 = fmaxf(mx2, __uint_as_float(sr[cc][e + 2]));
+          mx3 = fmaxf(mx3, __uint_as_float(sr[cc][e + 3]));
+        }
+      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+      const float m_new = fmaxf(m, mx * c);
+      const float m_use = m_new == -INFINITY ? 0.f : m_new;
+      const float alpha = ex2_approx(m - m_use);
+      if (j > 0) {
+        alpha_smem[s * kBM + r] = alpha;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(L::A_READY + s));
+      }
+      const float neg_m = -m_use;
+      float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc)
+#pragma unroll
+        for (int e = 0; e < 16; e += 4) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[cc][e + 0]), c, neg_m));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[cc][e + 1]), c, neg_m));
+          const float p2 = ex2_approx(fmaf(__uint_as_float(sr[cc][e + 2]), c, neg_m));
+          const float p3 = ex2_approx(fmaf(__uint_as_float(sr[cc][e + 3]), c, neg_m));
+          l0 += p0; l1 += p1; l2 += p2; l3 += p3;
+          sr[cc][e + 0] = __float_as_uint(p0);
+          sr[cc][e + 1] = __float_as_uint(p1);
+          sr[cc][e + 2] = __float_as_uint(p2);
+          sr[cc][e + 3] = __float_as_uint(p3);
+        }
+      l = l * alpha + ((l0 + l1) + (l2 + l3));
+      m = m_new;
+
+      // P_s(j-1) must have been consumed by PV_s(j-1) before it is replaced
+      if (j > 0 && !wait_bar_warp(bar(L::O_READY + s), (j - 1) & 1, ctl)) {
+        ok = false;
+        break;
+      }
+      // 16 chunks of 8 keys; chunk q lives in 64-key half q/8, swizzled
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const int cc = q >> 1, e0 = (q & 1) * 8;
+        const uint32_t w0 = pack2<BF16>(__uint_as_float(sr[cc][e0 + 0]), __uint_as_float(sr[cc][e0 + 1]));
+        const uint32_t w1 = pack2<BF16>(__uint_as_float(sr[cc][e0 + 2]), __uint_as_float(sr[cc][e0 + 3]));
+        const uint32_t w2 = pack2<BF16>(__uint_as_float(sr[cc][e0 + 4]), __uint_as_float(sr[cc][e0 + 5]));
+        const uint32_t w3 = pack2<BF16>(__uint_as_float(sr[cc][e0 + 6]), __uint_as_float(sr[cc][e0 + 7]));
+        const uint32_t addr = pbuf + static_cast<uint32_t>((q >> 3) * L::kBox + r * 128 +
+                                                           (((q & 7) ^ (r & 7)) << 4));
+        st_shared_v4(addr, w0, w1, w2, w3);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::P_FULL + s));
+    }
+
+    // ------------------------------ epilogue ------------------------------
+    if (ok) {
+      bool have_o = nT > 0;
+      if (have_o) {
+        have_o = wait_bar_warp(bar(L::O_READY + s), (nT - 1) & 1, ctl);
+        ok = have_o;
+      }
+      if (ok) {
+        tc_fence_after();
+        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        const uint32_t stage_buf = sQ + static_cast<uint32_t>(s * L::kQBytes);
+#pragma unroll 1
+        for (int cc = 0; cc < D / 16; ++cc) {
+          uint32_t v[16];
+          if (have_o) {
+            tmem_ld16(tO + cc * 16, v);
+            tmem_wait_ld();
+            reg_fence16(v);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = 0u;
+          }
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int col = cc * 16 + h * 8;  // first column of this chunk
+            const uint32_t w0 = pack2<BF16>(__uint_as_float(v[h * 8 + 0]) * inv_l, __uint_as_float(v[h * 8 + 1]) * inv_l);
+            const uint32_t w1 = pack2<BF16>(__uint_as_float(v[h * 8 + 2]) * inv_l, __uint_as_float(v[h * 8 + 3]) * inv_l);
+            const uint32_t w2 = pack2<BF16>(__uint_as_float(v[h * 8 + 4]) * inv_l, __uint_as_float(v[h * 8 + 5]) * inv_l);
+            const uint32_t w3 = pack2<BF16>(__uint_as_float(v[h * 8 + 6]) * inv_l, __uint_as_float(v[h * 8 + 7]) * inv_l);
+            const int box = col >> 6, chunk = (col & 63) >> 3;
+            const uint32_t addr = stage_buf + static_cast<uint32_t>(
+                                                  box * L::kBox + r * 128 + ((chunk ^ (r & 7)) << 4));
+            st_shared_v4(addr, w0, w1, w2, w3);
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        const int warp_row0 = stage_row0 + rq * 32;
+        if (lane == 0 && warp_row0 < p.Sq) {
+#pragma unroll
+          for (int box = 0; box < D / 64; ++box)
+            tma_store_3d(&tmO, stage_buf + static_cast<uint32_t>(box * L::kBox + rq * 32 * 128),
+                         box * 64, warp_row0, bh);
+          bulk_commit_group();
+          bulk_wait_group0();
+        }
+        if (row_g < p.Sq) {
+          const float lse = l > 0.f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+          p.lse[static_cast<size_t>(bh) * p.Sq + row_g] = lse;
+        }
+      }
+    }
+    __syncwarp();
+  } else if (wg == 2) {
+    // ============================== correction ==============================
+    const int rq = warp & 3;
+    const int r = rq * 32 + lane;
+    const uint32_t t_lane = static_cast<uint32_t>(rq * 32) << 16;
+#pragma unroll 1
+    for (int j = 1; j < n_kv; ++j) {
+      bool ok = true;
+#pragma unroll 1
+      for (int s = 0; s < 2; ++s) {
+        if (j >= (s == 0 ? nT0 : nT1)) continue;
+        if (!wait_bar_warp(bar(L::A_READY + s), (j - 1) & 1, ctl)) { ok = false; break; }
+        const float alpha = alpha_smem[s * kBM + r];
+        if (!wait_bar_warp(bar(L::O_READY + s), (j - 1) & 1, ctl)) { ok = false; break; }
+        tc_fence_after();
+        if (p.always_rescale || __any_sync(0xffffffffu, alpha != 1.f)) {
+          const uint32_t tO = tmem + t_lane + static_cast<uint32_t>(L::kTmemO + s * D);
+#pragma unroll 1
+          for (int cc = 0; cc < D / 16; ++cc) {
+            uint32_t v[16];
+            tmem_ld16(tO + cc * 16, v);
+            tmem_wait_ld();
+            reg_fence16(v);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+            tmem_st16(tO + cc * 16, v);
+          }
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(L::O_FIXED + s));
+      }
+      if (!ok) break;
+    }
+    __syncwarp();
+  } else if (warp == 12) {
+    // ============================== MMA issuer ==============================
+    if (lane == 0) {
+      constexpr uint32_t kIdescQK = idesc_f16(BF16, false, false, kBM, kBN);
+      constexpr uint32_t kIdescPV = idesc_f16(BF16, false, true, kBM, D);
+      const uint32_t tS0 = tmem, tS1 = tmem + kBN;
+      const uint32_t tO0 = tmem + L::kTmemO, tO1 = tmem + L::kTmemO + D;
+      bool issued = false;
+      bool ok = wait_bar(bar(L::Q_FULL + 0), 0, ctl) && wait_bar(bar(L::Q_FULL + 1), 0, ctl);
+
+      auto issue_qk = [&](uint32_t d_tmem, uint32_t qbuf, uint32_t kbuf) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = static_cast<uint32_t>((kk >> 2) * L::kBox + (kk & 3) * 32);
+          umma_f16_ss(d_tmem, smem_desc_sw128(qbuf + koff, 16, 1024),
+                      smem_desc_sw128(kbuf + koff, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](uint32_t d_tmem, uint32_t pbuf, uint32_t vbuf, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          const uint32_t poff = static_cast<uint32_t>((kk >> 2) * L::kBox + (kk & 3) * 32);
+          umma_f16_ss(d_tmem, smem_desc_sw128(pbuf + poff, 16, 1024),
+                      smem_desc_sw128(vbuf + static_cast<uint32_t>(kk * 16 * 128), L::kBox, 1024),
+                      kIdescPV, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      auto slot_of = [&](int fill) { return fill % L::kSlots; };
+      auto par_of = [&](int fill) { return static_cast<uint32_t>((fill / L::kSlots) & 1); };
+
+#pragma unroll 1
+      for (int j = 0; ok && j <= n_kv; ++j) {
+        const int fk = 2 * j, fv_prev = 2 * (j - 1) + 1, fv = 2 * j + 1;
+        if (j < n_kv) {
+          if (!wait_bar(bar(L::KV_FULL + slot_of(fk)), par_of(fk), ctl)) { ok = false; break; }
+          if (j < nT0) {
+            if (j > 0 && !wait_bar(bar(L::S_FREE + 0), (j - 1) & 1, ctl)) { ok = false; break; }
+            tc_fence_after();
+            issue_qk(tS0, sQ, sKV + slot_of(fk) * L::kKVBytes);
+            umma_commit(bar(L::S_FULL + 0));
+            issued = true;
+          }
+        }
+        if (j >= 1 && j - 1 < nT1) {  // PV_1(j-1)
+          if (!wait_bar(bar(L::KV_FULL + slot_of(fv_prev)), par_of(fv_prev), ctl) ||
+              !wait_bar(bar(L::P_FULL + 1), (j - 1) & 1, ctl) ||
+              (j - 1 >= 1 && !wait_bar(bar(L::O_FIXED + 1), (j - 2) & 1, ctl))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_pv(tO1, sP + L::kPBytes, sKV + slot_of(fv_prev) * L::kKVBytes, j - 1 > 0);
+          umma_commit(bar(L::O_READY + 1));
+          umma_commit(bar(L::KV_EMPTY + slot_of(fv_prev)));
+          issued = true;
+        }
+        if (j < n_kv) {
+          if (j > 0 && !wait_bar(bar(L::S_FREE + 1), (j - 1) & 1, ctl)) { ok = false; break; }
+          tc_fence_after();
+          issue_qk(tS1, sQ + L::kQBytes, sKV + slot_of(fk) * L::kKVBytes);
+          umma_commit(bar(L::S_FULL + 1));
+          umma_commit(bar(L::KV_EMPTY + slot_of(fk)));
+          issued = true;
+          if (j < nT0) {  // PV_0(j)
+            if (!wait_bar(bar(L::KV_FULL + slot_of(fv)), par_of(fv), ctl) ||
+                !wait_bar(bar(L::P_FULL + 0), j & 1, ctl) ||
+                (j >= 1 && !wait_bar(bar(L::O_FIXED + 0), (j - 1) & 1, ctl))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_pv(tO0, sP, sKV + slot_of(fv) * L::kKVBytes, j > 0);
+            umma_commit(bar(L::O_READY + 0));
+          }
+        }
+      }
+      if (issued) {  // every MMA issued so far completes before TMEM is freed
+        umma_commit(bar(L::DRAIN));
+        wait_drain(bar(L::DRAIN), 0, p.timeout_ns);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 13) {
+    // ============================== TMA producer =============================
+    if (lane == 0) {
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        mbar_arrive_expect_tx(bar(L::Q_FULL + s), L::kQBytes);
+#pragma unroll
+        for (int box = 0; box < D / 64; ++box)
+          tma_load_3d(sQ + static_cast<uint32_t>(s * L::kQBytes + box * L::kBox), &tmQ,
+                      bar(L::Q_FULL + s), box * 64, row0 + s * kBM, bh);
+      }
+      int fill = 0;
+      int last_fill[L::kSlots];
+#pragma unroll
+      for (int i = 0; i < L::kSlots; ++i) last_fill[i] = -1;
+      bool ok = true;
+#pragma unroll 1
+      for (int j = 0; ok && j < n_kv; ++j) {
+#pragma unroll 1
+        for (int kv = 0; kv < 2; ++kv, ++fill) {
+          const int slot = fill % L::kSlots;
+          const uint32_t par = static_cast<uint32_t>(((fill / L::kSlots) & 1) ^ 1);
+          if (!wait_bar(bar(L::KV_EMPTY + slot), par, ctl)) { ok = false; break; }
+          if (p.test_stall && fill == 2) continue;  // test hook: withhold K_1
+          mbar_arrive_expect_tx(bar(L::KV_FULL + slot), L::kKVBytes);
+          const CUtensorMap* tm = kv == 0 ? &tmK : &tmV;
+#pragma unroll
+          for (int box = 0; box < D / 64; ++box)
+            tma_load_3d(sKV + static_cast<uint32_t>(slot * L::kKVBytes + box * L::kBox), tm,
+                        bar(L::KV_FULL + slot), box * 64, j * kBN, bh);
+          last_fill[slot] = fill;
+        }
+      }
+      // drain: every load issued lands before shared memory goes away
+      wait_drain(bar(L::Q_FULL + 0), 0, p.timeout_ns);
+      wait_drain(bar(L::Q_FULL + 1), 0, p.timeout_ns);
+#pragma unroll
+      for (int i = 0; i < L::kSlots; ++i)
+        if (last_fill[i] >= 0)
+          wait_drain(bar(L::KV_FULL + i), static_cast<uint32_t>((last_fill[i] / L::kSlots) & 1),
+                     p.timeout_ns);
+    }
+    __syncwarp();
+  }
+
+  // ---- teardown ----
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 12) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::kTmemCols);
+  }
+}
+
+}  // namespace fa

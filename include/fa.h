@@ -1,0 +1,153 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) fused attention forward library,
+ * libfa_gb300.so.
+ *
+ * Operation (every entry point below computes it):
+ *   for each batch b, head h and query row i
+ *     O[b,h,i,:]  = sum_j softmax_j(scale * <Q[b,h,i,:], K[b,h,j,:]>) V[b,h,j,:]
+ *     LSE[b,h,i]  = ln sum_j exp(scale * <Q[b,h,i,:], K[b,h,j,:]>)
+ *   over the visible keys j: all of them, or, when causal, j <= i + (Skv - Sq)
+ *   (bottom-right alignment; equal to j <= i when Sq == Skv).  A row with no
+ *   visible key gets O = 0 and LSE = -inf.
+ *   This is the fused forward pass that "The FA5090 Optimization Journey"
+ *   (sections 2.2-2.8) and the B300 G5 page ("Flash Attention CUDA Kernel
+ *   optimisation: from 56 to 986 TFLOPS on B300", V21-V36) build: scores and
+ *   probabilities stay on chip, an online softmax carries the running row max
+ *   and row sum across key tiles.  LSE is the natural-log log-sum-exp of the
+ *   scaled scores; the pages do not define it, this library does.
+ *
+ * Layout and ownership (all device pointers are caller-owned CUDA memory on
+ * the current device; the library never frees or keeps them):
+ *   q   [B, H, Sq,  D]  contiguous, fp16 or bf16
+ *   k   [B, H, Skv, D]  contiguous, same type
+ *   v   [B, H, Skv, D]  contiguous, same type
+ *   o   [B, H, Sq,  D]  contiguous, same type (written)
+ *   lse [B, H, Sq]      contiguous, fp32 (written)
+ *   Every pointer must be 16-byte aligned.
+ *
+ * Supported: D in {64, 128}; dtype FA_F16 or FA_BF16; B*H < 65536;
+ * 1 <= Sq, Skv <= 2^24; scale finite and > 0.  A device that is not
+ * compute capability 10.3 (sm_103a) is rejected with FA_ERR_UNSUPPORTED.
+ *
+ * Errors: argument checks are synchronous and happen before anything is
+ * launched or allocated; a failed check returns its status and leaves every
+ * output untouched.  Launches are asynchronous on `stream`; a launch failure
+ * returns FA_ERR_CUDA.  Kernel-side waits are bounded: a wait that exceeds the
+ * watchdog limit (default 1 s) makes the kernel stop, release what it holds
+ * and record FA_ERR_TIMEOUT in a device status word, which
+ * fa_get_device_status() reports.  No entry point prints, throws or aborts.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *fa_stream_t;
+
+typedef enum { FA_F16 = 0, FA_BF16 = 1 } fa_dtype_t;
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size or scale   */
+  FA_ERR_UNSUPPORTED = 2, /* D, dtype or device not supported              */
+  FA_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed          */
+  FA_ERR_WORKSPACE = 4,   /* workspace missing, too small or misaligned    */
+  FA_ERR_TIMEOUT = 5      /* a kernel wait ran past the watchdog limit     */
+} fa_status_t;
+
+/* fa_fwd_ex flags */
+#define FA_FLAG_NO_LPT 0x1u          /* causal: plain CTA order instead of
+                                        heaviest-first (results are bitwise
+                                        identical either way)              */
+#define FA_FLAG_ALWAYS_RESCALE 0x2u  /* rescale O on every key tile, not only
+                                        when the row max changes (bitwise
+                                        identical either way)              */
+#define FA_FLAG_TEST_STALL 0x100u    /* test hook: the K/V producer withholds
+                                        its second tile, so the consumers'
+                                        bounded waits run out and the kernel
+                                        reports FA_ERR_TIMEOUT             */
+
+/*
+ * fa_fwd -- the whole forward pass for one batch, on `stream`.
+ * Prefill (Sq > 1): one fused kernel.  Decode (Sq == 1): split-KV kernel plus
+ * combine kernel, using a workspace that the library allocates on the first
+ * decode call on each device and keeps until process exit (use fa_fwd_ex to
+ * supply your own).
+ * Returns FA_OK once the work is enqueued.
+ */
+fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o,
+                   float *lse, int B, int H, int Sq, int Skv, int D,
+                   float scale, int causal, int dtype, fa_stream_t stream);
+
+/*
+ * fa_workspace_bytes -- bytes of device workspace fa_fwd_ex needs for this
+ * shape with `num_splits` key splits (0 = the library's choice); 0 when the
+ * shape needs none.  The split-KV partials are fp32 (O, LSE) per split: the
+ * fp32 workspace round trip that "The FA5090 Optimization Journey" section 2.7
+ * measured (and rejected for prefill); here it serves only decode, where one
+ * query row per head leaves too few work items to fill the GPU otherwise.
+ */
+size_t fa_workspace_bytes(int B, int H, int Sq, int Skv, int D,
+                          int num_splits);
+
+/*
+ * fa_fwd_ex -- fa_fwd with explicit options.
+ *   flags       FA_FLAG_* bits above (0 for the default path)
+ *   num_splits  decode key splits; 0 = the library's choice, 1 = no split
+ *   workspace   caller-owned device memory, 256-byte aligned, at least
+ *               fa_workspace_bytes(...) bytes; may be NULL when that is 0.
+ *               It must not be used by anything else until the work on
+ *               `stream` has finished.
+ * Allocates nothing.
+ */
+fa_status_t fa_fwd_ex(const void *q, const void *k, const void *v, void *o,
+                      float *lse, int B, int H, int Sq, int Skv, int D,
+                      float scale, int causal, int dtype, unsigned flags,
+                      int num_splits, void *workspace, size_t workspace_bytes,
+                      fa_stream_t stream);
+
+/*
+ * fa_host_staging_bytes / fa_fwd_host -- the same operation on HOST buffers.
+ * q_h, k_h, v_h, o_h, lse_h are host pointers (pinned memory gives full copy
+ * bandwidth; pageable memory works but is slower).  `staging` is caller-owned
+ * device memory of at least fa_host_staging_bytes(...) bytes, 256-byte
+ * aligned: the library copies Q, K, V into it, runs the forward pass there
+ * and copies O and LSE back, all on `stream`.  The call returns once the
+ * work is enqueued; the host outputs are valid after the stream synchronises.
+ * Allocates nothing.
+ */
+size_t fa_host_staging_bytes(int B, int H, int Sq, int Skv, int D);
+fa_status_t fa_fwd_host(const void *q_h, const void *k_h, const void *v_h,
+                        void *o_h, float *lse_h, int B, int H, int Sq,
+                        int Skv, int D, float scale, int causal, int dtype,
+                        void *staging, size_t staging_bytes,
+                        fa_stream_t stream);
+
+/*
+ * fa_get_device_status -- synchronises `stream`, then returns and clears the
+ * device status word of the current device: FA_OK, or FA_ERR_TIMEOUT if a
+ * kernel's bounded wait ran out since the last call.  FA_ERR_CUDA if the
+ * synchronisation itself failed.
+ */
+fa_status_t fa_get_device_status(fa_stream_t stream);
+
+/* Watchdog limit for every kernel-side wait, in nanoseconds (default 1e9).
+ * Applies to launches made after the call.  0 restores the default. */
+void fa_set_watchdog_ns(unsigned long long ns);
+
+/* Static description of a status code (never NULL). */
+const char *fa_status_string(fa_status_t status);
+
+/* Library ABI version: major * 10000 + minor * 100 + patch. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

@@ -1,0 +1,105 @@
+"""The C-ABI library: it builds, loads, exports every entry point that
+include/fa.h declares, and rejects bad arguments before touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from attention_forward_gb300 import _build, fa
+    _build.build()
+    return fa.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w\s\*]*?\b(fa_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("fa_fwd", "fa_fwd_ex", "fa_workspace_bytes", "fa_fwd_host",
+              "fa_host_staging_bytes", "fa_get_device_status",
+              "fa_set_watchdog_ns", "fa_status_string", "fa_version"):
+        assert n in names, n
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), f"{n} declared in fa.h but not exported"
+
+
+def test_status_strings_and_version(lib):
+    from attention_forward_gb300 import fa
+    for st in range(6):
+        assert fa.fa_status_string(st)
+    assert fa.fa_status_string(99) == "unknown status"
+    assert fa.fa_version() == 10000
+
+
+def _call(lib, q=16, k=16, v=16, o=16, lse=16, B=1, H=1, Sq=8, Skv=8, D=64,
+          scale=0.125, causal=0, dtype=1):
+    return lib.fa_fwd(q, k, v, o, lse, B, H, Sq, Skv, D, scale, causal, dtype,
+                      None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(q=0), 1), (dict(o=0), 1), (dict(lse=0), 1),
+    (dict(k=24), 1), (dict(v=8), 1),                  # misaligned
+    (dict(B=0), 1), (dict(H=-1), 1), (dict(Sq=0), 1), (dict(Skv=0), 1),
+    (dict(B=256, H=256), 1), (dict(Sq=(1 << 24) + 1), 1),
+    (dict(scale=0.0), 1), (dict(scale=-1.0), 1), (dict(scale=float("inf")), 1),
+    (dict(scale=float("nan")), 1),
+    (dict(D=96), 2), (dict(D=256), 2), (dict(dtype=2), 2), (dict(dtype=-1), 2),
+])
+def test_argument_errors_precede_any_cuda_call(lib, kw, want):
+    """Validation happens before the device is touched, so it answers the
+    same on a machine without a GPU."""
+    assert _call(lib, **kw) == want
+
+
+def test_workspace_and_staging_sizes(lib):
+    from attention_forward_gb300 import fa
+    assert fa.fa_workspace_bytes(1, 1, 128, 128, 128) == 0   # prefill: none
+    assert fa.fa_workspace_bytes(1, 1, 1, 8192, 128, 1) == 0  # one split
+    n = fa.fa_workspace_bytes(2, 3, 1, 1000, 128, 4)
+    per = 2 * 3 * 4
+    assert n >= per * 128 * 4 + per * 4 and n % 256 == 0
+    assert fa.fa_host_staging_bytes(1, 2, 128, 256, 64) >= (
+        2 * 128 * 64 * 2 * 2 + 2 * 2 * 256 * 64 * 2 + 2 * 128 * 4)
+
+
+def test_binding_rejects_bad_tensors():
+    from attention_forward_gb300 import fa
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.fa_fwd(q, q.float(), q)
+    with pytest.raises(ValueError):
+        fa.fa_fwd(q, q[:, :, :, :32], q)
+    with pytest.raises(ValueError):
+        fa.fa_fwd(q.transpose(2, 3), q, q)
+
+
+def test_product_path_does_not_touch_the_oracle():
+    """The library and its binding never load the oracle: no import of it in
+    the package, and no oracle symbol in the shared object."""
+    pkg = os.path.join(ROOT, "attention_forward_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in src and "from oracle" not in src, f
+                assert "liboracle" not in src, f
+    from attention_forward_gb300 import _build
+    _build.build()
+    data = open(_build.LIB, "rb").read()
+    assert b"oracle_attention_rows" not in data

@@ -1,0 +1,150 @@
+"""Parity of the CUDA path (called through the C ABI) with the fp64 oracle,
+on the workloads of the build and on edge cases.  Gate: oracle/gate.py."""
+import numpy as np
+import pytest
+import torch
+
+from attention_forward_gb300 import fa, inputs
+from parity import check, run_and_check, run_kernel, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+    assert torch.cuda.is_available()
+
+
+def _assert(r):
+    assert r.passed, str(r)
+
+
+def test_pr1():
+    w = inputs.PR1
+    _assert(run_and_check(w.B, w.H, w.Sq, w.Skv, w.D, w.dtype, w.causal, w.seed))
+
+
+@pytest.mark.parametrize("w", [inputs.C2, inputs.C2_CAUSAL, inputs.C2_X4,
+                               inputs.C2_X4_CAUSAL], ids=lambda w: w.name)
+def test_c2_all_rows(w):
+    _assert(run_and_check(w.B, w.H, w.Sq, w.Skv, w.D, w.dtype, w.causal,
+                          w.seed, w.qk_mult))
+
+
+EDGE = [  # B, H, Sq, Skv, D, dtype, causal
+    (1, 1, 2, 2, 64, "bf16", False), (1, 1, 2, 2, 128, "fp16", True),
+    (1, 1, 7, 7, 128, "bf16", True), (2, 3, 127, 127, 64, "fp16", False),
+    (1, 2, 128, 128, 128, "bf16", True), (1, 2, 129, 129, 128, "bf16", True),
+    (1, 1, 255, 255, 64, "bf16", True), (1, 1, 256, 256, 128, "fp16", True),
+    (1, 1, 257, 257, 128, "bf16", False), (2, 2, 300, 300, 64, "bf16", True),
+    (1, 2, 1000, 1000, 128, "fp16", True), (1, 1, 100, 300, 128, "bf16", True),
+    (1, 1, 100, 300, 64, "fp16", False), (1, 1, 300, 100, 128, "bf16", True),
+    (1, 1, 300, 100, 64, "bf16", False), (1, 1, 513, 1, 128, "bf16", False),
+    (1, 1, 600, 129, 128, "fp16", True), (3, 1, 384, 640, 64, "bf16", True),
+]
+
+
+@pytest.mark.parametrize("case", EDGE, ids=lambda c: "x".join(map(str, c)))
+def test_edge_shapes(case):
+    B, H, Sq, Skv, D, dt, causal = case
+    _assert(run_and_check(B, H, Sq, Skv, D, dt, causal, 11, qk_mult=2.0))
+
+
+def test_headline_sampled_rows():
+    """B4 H16 S4096 D128 bf16 non-causal at full size, in the launch the bench
+    times (fa_fwd, default options); >= 512 sampled rows covering every head."""
+    w = inputs.HEADLINE
+    rows = sample_rows(w.B, w.H, w.Sq, per_head=8, extra=256, seed=1)
+    assert rows.size >= 512
+    _assert(run_and_check(w.B, w.H, w.Sq, w.Skv, w.D, w.dtype, w.causal,
+                          w.seed, rows=rows))
+
+
+@pytest.mark.parametrize("w", [inputs.LONG16K, inputs.LONG32K],
+                         ids=lambda w: w.name)
+def test_long_causal_sampled_rows(w):
+    rows = sample_rows(w.B, w.H, w.Sq, per_head=24, extra=128, seed=2)
+    _assert(run_and_check(w.B, w.H, w.Sq, w.Skv, w.D, w.dtype, w.causal,
+                          w.seed, rows=rows))
+
+
+@pytest.mark.parametrize("w", inputs.SWEEP, ids=lambda w: w.name)
+def test_sweep_sampled_rows(w):
+    rows = sample_rows(w.B, w.H, w.Sq, per_head=2, extra=64, seed=3)
+    _assert(run_and_check(w.B, w.H, w.Sq, w.Skv, w.D, w.dtype, w.causal,
+                          w.seed, rows=rows))
+
+
+def test_decode_all_rows():
+    """Sq=1, Skv=8192, B32 H32 D128 bf16: every output row, the default
+    split count (the bench's launch)."""
+    w = inputs.DECODE
+    _assert(run_and_check(w.B, w.H, w.Sq, w.Skv, w.D, w.dtype, w.causal,
+                          w.seed))
+
+
+@pytest.mark.parametrize("num_splits", [1, 2, 3, 7])
+@pytest.mark.parametrize("D,dt,Skv", [(128, "bf16", 1000), (64, "fp16", 513),
+                                      (128, "fp16", 64), (64, "bf16", 3)])
+def test_decode_splits(num_splits, D, dt, Skv):
+    q, k, v = inputs.make_qkv(2, 5, 1, Skv, D, dt, 21, 3.0)
+    ws_bytes = fa.fa_workspace_bytes(2, 5, 1, Skv, D, num_splits)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device="cuda")
+    o, lse = run_kernel(q, k, v, False, num_splits=num_splits, workspace=ws)
+    _assert(check(q, k, v, o, lse, False, dt))
+
+
+def test_repeat_lpt_and_rescale_switches_are_bitwise_identical():
+    q, k, v = inputs.make_qkv(2, 4, 1000, 1000, 128, "bf16", 5, 4.0)
+    o1, l1 = run_kernel(q, k, v, True)
+    o2, l2 = run_kernel(q, k, v, True)
+    o3, l3 = run_kernel(q, k, v, True, flags=fa.FA_FLAG_NO_LPT)
+    o4, l4 = run_kernel(q, k, v, True, flags=fa.FA_FLAG_ALWAYS_RESCALE)
+    for o, l in ((o2, l2), (o3, l3), (o4, l4)):
+        assert torch.equal(o, o1) and torch.equal(l, l1)
+
+
+def test_concurrent_streams_bitwise_identical():
+    q, k, v = inputs.make_qkv(2, 8, 1024, 1024, 128, "bf16", 6)
+    dq, dk, dv = (t.cuda() for t in (q, k, v))
+    ref, lref = fa.fa_fwd(dq, dk, dv, causal=True)
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    outs = []
+    for s in streams:
+        with torch.cuda.stream(s):
+            outs.append(fa.fa_fwd(dq, dk, dv, causal=True, stream=s))
+    torch.cuda.synchronize()
+    for o, l in outs:
+        assert torch.equal(o, ref) and torch.equal(l, lref)
+
+
+def test_host_buffers_path_matches_device_path():
+    for (Sq, Skv, causal) in ((300, 300, True), (1, 700, False)):
+        q, k, v = inputs.make_qkv(2, 3, Sq, Skv, 128, "bf16", 7)
+        o_d, l_d = run_kernel(q, k, v, causal)
+        pin = [t.pin_memory() for t in (q, k, v)]
+        staging = torch.empty(fa.fa_host_staging_bytes(2, 3, Sq, Skv, 128),
+                              dtype=torch.uint8, device="cuda")
+        o_h, l_h = fa.fa_fwd_host(*pin, staging, causal=causal)
+        torch.cuda.synchronize()
+        assert torch.equal(o_h, o_d.cpu()) and torch.equal(l_h, l_d.cpu())
+
+
+def test_watchdog_reports_timeout_and_context_survives():
+    """The test hook withholds one K/V tile: the consumers' bounded waits run
+    out, the kernel stops and reports FA_ERR_TIMEOUT, and the next call on the
+    same context is correct."""
+    q, k, v = inputs.make_qkv(1, 2, 256, 512, 128, "bf16", 8)
+    dq, dk, dv = (t.cuda() for t in (q, k, v))
+    assert fa.fa_get_device_status() == fa.FA_OK
+    fa.fa_set_watchdog_ns(20_000_000)  # 20 ms
+    try:
+        fa.fa_fwd_ex(dq, dk, dv, flags=fa.FA_FLAG_TEST_STALL)
+        assert fa.fa_get_device_status() == fa.FA_ERR_TIMEOUT
+        assert fa.fa_get_device_status() == fa.FA_OK  # cleared
+    finally:
+        fa.fa_set_watchdog_ns(0)
+    o, lse = run_kernel(q, k, v, False)
+    _assert(check(q, k, v, o, lse, False, "bf16"))
