@@ -356,11 +356,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ------------------------------ epilogue ------------------------------
     if (ok) {
-      bool have_o = nT > 0;
-      if (have_o) {
-        have_o = wait_bar_warp(bar(L::O_READY + s), (nT - 1) & 1, ctl);
-        ok = have_o;
-      }
+      const bool have_o = nT > 0;
+      // the Q_s buffer becomes the output staging buffer: its TMA load must
+      // have landed (a stage with no key tile never waited for it), and the
+      // last PV_s must have completed (it also ends every QK_s read of Q_s)
+      ok = wait_bar_warp(bar(L::Q_FULL + s), 0, ctl);
+      if (ok && have_o) ok = wait_bar_warp(bar(L::O_READY + s), (nT - 1) & 1, ctl);
       if (ok) {
         tc_fence_after();
         const float inv_l = l > 0.f ? 1.f / l : 0.f;

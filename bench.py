@@ -1,0 +1,461 @@
+"""Throughput of the fused attention forward pass on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+A step is one forward pass (every step of the hot path) over one batch of
+synthetic input already resident in HBM.  The default workload is
+B=4, H=16, Sq=Skv=4096, D=128, bf16, non-causal.  Rank 0 prints one JSON line.
+
+Multi-GPU (torchrun, one process per GPU): every rank runs its own batch of
+the same shape (independent heads, no data-path collective), so scaling is
+weak; the time is the max over ranks and the value is all ranks' FLOPs over
+that time.
+
+--impl reference times the CPU oracle (oracle/, fp64 three-step attention) on
+the host cores, on a bounded row sample of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from attention_forward_gb300 import inputs  # noqa: E402
+
+METRIC = "attention fwd TFLOP/s (4*B*H*Sq*Skv*D, 1/2 causal)"
+UNIT = "TFLOP/s"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
+                  "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=inputs.HEADLINE.name,
+                    choices=sorted(inputs.BY_NAME))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-gemm-ceiling", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target CPU time of the oracle baseline sample")
+    return ap.parse_args(argv)
+
+
+# ----------------------------------------------------------------- helpers
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def shard_seed(seed: int, rank: int) -> int:
+    """Each rank draws its own batch (weak scaling)."""
+    return seed + 1000 * rank
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_fingerprint() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "attention_forward_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kind: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources and this workload; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = d.get(kind, {})
+    if e.get("kernel_fingerprint") != kernel_fingerprint() or e.get("workload") != workload:
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons, stamped on arrival."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "20", "-i", gpu_id],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        inside = [s for t, s in self.samples if t0 <= t <= t1]
+        note = "inside timed region"
+        if not inside and self.samples:
+            near = sorted(self.samples, key=lambda ts: min(abs(ts[0] - t0), abs(ts[0] - t1)))
+            inside = [s for _, s in near[:3]]
+            note = "nearest samples (timed region shorter than the sampling period)"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        mhz, mx, pw = [], [], []
+        for s in inside:
+            try:
+                mhz.append(float(s[0]))
+                mx.append(float(s[1]))
+                pw.append(float(s[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, s[4:8]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_median": statistics.median(pw) if pw else None,
+                "reasons": sorted(reasons), "samples": len(inside), "note": note}
+
+
+def gpu_id_for_smi(device) -> str:
+    props = torch.cuda.get_device_properties(device)
+    bus = getattr(props, "pci_bus_id", None)
+    dom = getattr(props, "pci_domain_id", None)
+    dev = getattr(props, "pci_device_id", None)
+    if bus is not None and dom is not None and dev is not None:
+        return f"{dom:08X}:{bus:02X}:{dev:02X}.0"
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids = [x for x in vis.split(",") if x.strip()]
+    if ids and ids[device.index if device.index is not None else 0].strip().isdigit():
+        return ids[device.index or 0].strip()
+    return str(device.index or 0)
+
+
+def gemm_ceiling(device) -> float:
+    """Dense bf16 GEMM throughput in this run (torch.matmul 8192^3, best of
+    10): the ceiling the attention kernel is compared with."""
+    n = 8192
+    a = torch.randn(n, n, device=device, dtype=torch.bfloat16)
+    b = torch.randn(n, n, device=device, dtype=torch.bfloat16)
+    for _ in range(3):
+        torch.matmul(a, b)
+    torch.cuda.synchronize(device)
+    best = float("inf")
+    for _ in range(10):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        torch.matmul(a, b)
+        e.record()
+        e.synchronize()
+        best = min(best, s.elapsed_time(e) / 1e3)
+    del a, b
+    return 2.0 * n ** 3 / best / 1e12
+
+
+# ------------------------------------------------------------ CPU (oracle)
+
+class OracleSample:
+    """The fp64 oracle timed on a row sample of the workload (host cores).
+    The per-row cost is 4*Skv*D FLOPs (the visible keys for causal rows)."""
+
+    def __init__(self, w: inputs.Workload, seed: int = 0):
+        import oracle
+        self.oracle = oracle
+        self.w = w
+        self.nthreads = oracle.default_threads()
+        self.rng = np.random.default_rng(seed)
+        heads = sorted(set(int(x) for x in self.rng.integers(0, w.B * w.H, size=4)))
+        self.nh = len(heads)
+        q, k, v = w.make(heads=heads)
+        self.q, self.k, self.v = (t.float().numpy()[None] for t in (q, k, v))
+
+    def _flops(self, rows):
+        w = self.w
+        i = rows % w.Sq
+        if w.causal:
+            vis = np.minimum(w.Skv, i + (w.Skv - w.Sq) + 1).clip(min=0)
+        else:
+            vis = np.full(rows.shape, w.Skv)
+        return float((4.0 * vis * w.D).sum())
+
+    def run(self, n: int):
+        rows = self.rng.integers(0, self.nh * self.w.Sq, size=n)
+        t = time.perf_counter()
+        self.oracle.attention(self.q, self.k, self.v, self.w.scale, self.w.causal,
+                              rows=rows, nthreads=self.nthreads)
+        return time.perf_counter() - t, self._flops(rows)
+
+    def rows_for(self, target_s: float) -> int:
+        n = max(self.nthreads, 8)
+        dt, _ = self.run(n)
+        while dt < 0.25 and n < (1 << 20):
+            n *= 4
+            dt, _ = self.run(n)
+        return max(self.nthreads, int(n * target_s / max(dt, 1e-6)))
+
+    def describe(self, n: int) -> str:
+        return (f"{n} query rows (all their visible keys) drawn from {self.nh} heads of "
+                f"{self.w.name}, fp64, {self.nthreads} threads")
+
+
+def oracle_rate(w: inputs.Workload, target_s: float):
+    """(TFLOP/s, cores, sample, seconds) of the oracle on about target_s of work."""
+    smp = OracleSample(w)
+    n = smp.rows_for(target_s)
+    dt, fl = smp.run(n)
+    return fl / dt / 1e12, smp.nthreads, smp.describe(n), dt
+
+
+# ------------------------------------------------------------------ arms
+
+def bench_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    # each step: a bounded row sample, sized so the whole run stays near a
+    # couple of minutes
+    smp = OracleSample(w)
+    per_step = min(10.0, max(0.02, 120.0 / max(1, args.steps + args.warmup)))
+    n = smp.rows_for(per_step)
+    for _ in range(args.warmup):
+        smp.run(n)
+    secs, flops = 0.0, 0.0
+    for _ in range(args.steps):
+        dt, fl = smp.run(n)
+        secs += dt
+        flops += fl
+    value = flops / secs / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w, 1),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": smp.nthreads,
+                         "kind": "oracle", "sample": "each step: " + smp.describe(n)},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w, n_gpus):
+    return {"workload": w.name, "B": w.B, "H": w.H, "Sq": w.Sq, "Skv": w.Skv, "D": w.D,
+            "causal": w.causal, "global_batch": w.B * n_gpus, "seq_len": w.Skv,
+            "parallelism": f"independent batches x{n_gpus}"}
+
+
+def bench_ours(args, w):
+    from attention_forward_gb300 import fa
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    fa.load()
+
+    q, k, v = inputs.make_qkv(w.B, w.H, w.Sq, w.Skv, w.D, w.dtype,
+                              shard_seed(w.seed, rank), w.qk_mult)
+    dq, dk, dv = (t.to(device) for t in (q, k, v))
+    o = torch.empty_like(dq)
+    lse = torch.empty((w.B, w.H, w.Sq), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    decode = w.Sq == 1
+
+    def step():
+        fa.fa_fwd(dq, dk, dv, causal=w.causal, out=o, lse=lse, stream=stream)
+
+    launches_per_step = 1
+    if decode:
+        launches_per_step = 2 if fa.fa_workspace_bytes(w.B, w.H, 1, w.Skv, w.D) > 0 else 1
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(device)
+    if fa.fa_get_device_status() != fa.FA_OK:
+        raise RuntimeError("kernel watchdog fired during warm-up")
+
+    sampler = ClockSampler(gpu_id_for_smi(device))
+    time.sleep(0.3)
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world, device)
+    torch.cuda.synchronize(device)
+    wall0 = time.time()
+    t_start.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(device)
+    wall1 = time.time()
+    barrier(world, device)
+    sampler.stop()
+    if fa.fa_get_device_status() != fa.FA_OK:
+        raise RuntimeError("kernel watchdog fired in the timed region")
+
+    total_s = t_start.elapsed_time(t_end) / 1e3
+    launch_s = statistics.mean(a.elapsed_time(b) for a, b in ev) / 1e3
+    total_max = max_over_ranks(total_s, world, device)
+    flops_step = w.flops()
+    value = flops_step * K * world / total_max / 1e12
+
+    peaks, peak_src = load_peaks()
+    if decode:
+        # algorithmic bytes: read Q, K, V once, write O and LSE
+        nbytes = (w.B * w.H * (w.Sq + 2 * w.Skv) * w.D * 2 + w.B * w.H * w.Sq * w.D * 2
+                  + w.B * w.H * w.Sq * 4)
+        achieved = nbytes / launch_s / 1e9
+        peak = float(peaks["hbm_gbs"])
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": profiled_traffic("decode", w.name),
+                "peak_source": f"{peak_src} hbm_gbs",
+                "kernel": "fa_decode_kernel + fa_decode_combine_kernel (one step)"}
+    else:
+        achieved = flops_step / launch_s / 1e12
+        peak = float(peaks["bf16_tflops"])
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": profiled_traffic("prefill", w.name),
+                "peak_source": f"{peak_src} bf16_tflops (burst; dense fp16 has the same rate)",
+                "kernel": "fa_prefill_kernel"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": total_max / K * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic (seeded N(0,1), per-rank batches)",
+        "config": dict(workload_config(w, world),
+                       l2=f"inputs {3 * dq.numel() * 2 / 2**20:.0f} MiB "
+                          f"{'>' if 3 * dq.numel() * 2 > L2_BYTES else '<='} L2 129 MiB; no flush"),
+        "roofline": roof,
+        "gpu_launches": K * launches_per_step,
+        "clocks": sampler.summary(wall0, wall1),
+    }
+
+    if not args.no_e2e:
+        line["e2e"] = e2e(w, q, k, v, device, stream, min(K, 20))
+    if rank == 0 and world == 1 and not args.no_gemm_ceiling:
+        g = gemm_ceiling(device)
+        line["gemm_ceiling_tflops_same_run"] = g
+        line["frac_of_same_run_gemm"] = roof["achieved"] / g if not decode else None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r, cores, sample, dt = oracle_rate(w, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": r, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": sample, "seconds": dt}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def e2e(w, q, k, v, device, stream, n_steps):
+    """Same metric through the host-buffer C-ABI call: every step copies Q,
+    K, V from pinned host memory, runs, and copies O and LSE back."""
+    from attention_forward_gb300 import fa
+    qh, kh, vh = (t.pin_memory() for t in (q, k, v))
+    oh = torch.empty_like(qh).pin_memory()
+    lh = torch.empty((w.B, w.H, w.Sq), dtype=torch.float32).pin_memory()
+    staging = torch.empty(fa.fa_host_staging_bytes(w.B, w.H, w.Sq, w.Skv, w.D),
+                          dtype=torch.uint8, device=device)
+    for _ in range(2):
+        fa.fa_fwd_host(qh, kh, vh, staging, causal=w.causal, out_h=oh, lse_h=lh,
+                       stream=stream)
+    torch.cuda.synchronize(device)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(n_steps):
+        fa.fa_fwd_host(qh, kh, vh, staging, causal=w.causal, out_h=oh, lse_h=lh,
+                       stream=stream)
+    e.record(stream)
+    torch.cuda.synchronize(device)
+    sec = s.elapsed_time(e) / 1e3 / n_steps
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
+    d2h = oh.numel() * oh.element_size() + lh.numel() * 4
+    return {"value": w.flops() / sec / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": sec * 1e3, "steps": n_steps,
+            "api": "fa_fwd_host (pinned host buffers, copies inside the timed region)"}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    w = inputs.BY_NAME[args.workload]
+    if args.impl == "reference":
+        return bench_reference(args, w)
+    return bench_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
