@@ -59,6 +59,9 @@ def load() -> ctypes.CDLL:
     L.fa_fwd_host.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci,
                               ci, vp, sz, vp]
     L.fa_fwd_host.restype = ci
+    L.fa_fwd_decode_static.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, cf,
+                                       ci, vp]
+    L.fa_fwd_decode_static.restype = ci
     L.fa_get_device_status.argtypes = [vp]
     L.fa_get_device_status.restype = ci
     L.fa_set_watchdog_ns.argtypes = [ctypes.c_ulonglong]
@@ -175,6 +178,24 @@ def fa_fwd_host(q_h, k_h, v_h, staging, causal: bool = False,
                             _stream_handle(stream))
     _check(st, "fa_fwd_host")
     return out_h, lse_h
+
+
+def fa_fwd_decode_static(q, k, v, scale: float | None = None, out=None,
+                         lse=None, stream=None):
+    """Decode (Sq == 1) without any device allocation: the split partials go
+    to the library's static device scratch.  Calls whose GPU work overlaps
+    share that scratch and race.  Returns (o, lse)."""
+    B, H, Sq, Skv, D = _shape(q, k, v)
+    if Sq != 1:
+        raise ValueError("fa_fwd_decode_static takes one query row per head")
+    out, lse = _outputs(q, out, lse)
+    sc = float(D) ** -0.5 if scale is None else float(scale)
+    st = load().fa_fwd_decode_static(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                     out.data_ptr(), lse.data_ptr(), B, H, Skv,
+                                     D, sc, _DTYPE[q.dtype],
+                                     _stream_handle(stream))
+    _check(st, "fa_fwd_decode_static")
+    return out, lse
 
 
 def fa_get_device_status(stream=None) -> int:

@@ -129,6 +129,35 @@ fa_status_t fa_fwd_host(const void *q_h, const void *k_h, const void *v_h,
                         fa_stream_t stream);
 
 /*
+ * fa_fwd_decode_static -- the decode pass (one query row per head, Sq = 1)
+ * for callers that cannot allocate device memory: host frameworks that own
+ * every device allocation and forbid side allocations, serving loops that
+ * must not meet cudaMalloc's implicit device synchronisation or its run-time
+ * failure, processes with a memory budget fixed up front.  The pages have no
+ * counterpart; this is a deployment entry point of this library.
+ *   q [B,H,1,D], k and v [B,H,Skv,D], o [B,H,1,D], lse [B,H,1]: caller-owned
+ *   device memory as for fa_fwd.  Every key is visible (for one query row the
+ *   causal and full masks agree).
+ * The split-KV partials go to a static device array of
+ * FA_DECODE_STATIC_SCRATCH_BYTES that is part of the library's module: every
+ * GPU that loads the library holds it until the process exits.  The partials
+ * need n_splits * B * H * (D + 1) * 4 bytes (about, rounded up; n_splits is
+ * the library's choice, fa_workspace_bytes(B, H, 1, Skv, D, 0) gives the
+ * exact figure); a shape that needs more returns FA_ERR_WORKSPACE before
+ * anything is launched.  Nothing in the array has to start at zero.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Calls share the one array: two calls whose work overlaps on the
+ * GPU (different streams, or different host threads) race and corrupt each
+ * other's results.  Allocates nothing.
+ */
+#define FA_DECODE_STATIC_SCRATCH_BYTES (8u << 20)
+fa_status_t fa_fwd_decode_static(const void *q, const void *k, const void *v,
+                                 void *o, float *lse, int B, int H, int Skv,
+                                 int D, float scale, int dtype,
+                                 fa_stream_t stream);
+
+/*
  * fa_get_device_status -- synchronises `stream`, then returns and clears the
  * device status word of the current device: FA_OK, or FA_ERR_TIMEOUT if a
  * kernel's bounded wait ran out since the last call.  FA_ERR_CUDA if the
