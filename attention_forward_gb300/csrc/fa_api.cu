@@ -189,6 +189,7 @@ fa_status_t run_prefill(DeviceState& d, const void* q, const void* k, const void
   p.always_rescale = (flags & FA_FLAG_ALWAYS_RESCALE) ? 1 : 0;
   p.test_stall = (flags & FA_FLAG_TEST_STALL) ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.rescale_tau = (flags & FA_FLAG_EXACT_MAX) ? 0.f : 8.f;
   const long long grid = static_cast<long long>(p.n_qtiles) * BH;
   if (grid > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
   if (fa::launch_prefill(D, bf16, tq, tk, tv, to, p, static_cast<int>(grid), stream) !=

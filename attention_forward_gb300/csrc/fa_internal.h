@@ -30,6 +30,7 @@ struct PrefillParams {
   int always_rescale;
   int test_stall;
   float scale_log2;           // scale * log2(e)
+  float rescale_tau;          // raise the reference max only past this (log2)
 };
 
 // Decode (Sq == 1) split-KV.

@@ -6,38 +6,42 @@
 //
 //   warps 0-3   softmax, stage 0   one thread per query row (TMEM lane)
 //   warps 4-7   softmax, stage 1
-//   warps 8-11  correction: rescales O in TMEM when a row max moved
+//   warps 8-11  correction: rescales O in TMEM when a row's reference max moved
 //   warp  12    tcgen05.mma issuer (one thread) + TMEM allocation
 //   warp  13    TMA producer (one thread): Q once, then K/V tiles
 //   warps 14-15 idle (they complete the fourth warpgroup)
 //
-// Per stage s the tensor memory holds S_s = Q_s K^T (128 fp32 columns) and
-// the output accumulator O_s (D fp32 columns): 2*128 + 2*D <= 512 columns.
-// P goes through shared memory in the tensor core's K-major 128-byte swizzled
-// layout (the smem_P choice of the G5 page), so both GEMMs read operands
-// from shared memory.
+// Tensor memory (512 columns x 128 lanes): S_s = Q_s K^T at columns s*128
+// (fp32), O_s at 256 + s*D (fp32).  Softmax writes P_s as packed 16-bit
+// pairs over the first 64 columns of S_s, and PV reads its A operand from
+// there (P never touches shared memory).  The next S_s overwrites P_s; the
+// single MMA thread issues PV_s(j) before QK_s(j+1) and the tensor core
+// executes one thread's MMAs in issue order.
 //
 // Issue order of the tensor core, per key tile j:
 //     QK_0(j)  PV_1(j-1)  QK_1(j)  PV_0(j)
 // so that each softmax warpgroup has two GEMMs of the other stage to hide
-// behind (the aim of the ping-pong on the G5 page).  K and V use separate
+// behind (the aim of the ping-pong on the G5 page).  K and V occupy separate
 // slots of one ring with their own full/empty barriers (the decoupled K/V
-// loads of G5 V26), the score buffer is released as soon as softmax has
-// read it (the separate "score free" barrier of V28), and stage 0's PV does
-// not wait for stage 1 (the PV0 barrier of V30).
+// loads of G5 V26), and stage 0's PV never waits for stage 1 (the PV0
+// barrier of V30).
 //
 // Softmax works in the log2 domain with the scale folded into one FFMA
 // before ex2 (G5 V33 "log2exp2"; "The FA5090 Optimization Journey" section
-// 2.6): t = s*scale*log2(e), m = running max of t, p = 2^(t - m).
-// The correction warpgroup multiplies O by alpha = 2^(m_old - m_new) only
-// when some row of its warp changed its max (alpha != 1): the identity
-// rescale skip of the FA5090 page section 2.8, with the warp-uniform vote it
-// describes; skipping a multiply by exactly 1 is bitwise neutral.
+// 2.6): t = s*scale*log2(e), p = 2^(t - m) against a per-row reference max m.
+// m is raised only when the tile's max exceeds it by more than tau (log2
+// units); then alpha = 2^(m_old - m_new) and the correction warpgroup
+// multiplies O by alpha, skipping any warp whose 32 rows all have alpha == 1
+// (a warp-uniform vote).  tau = 0 is the identity-only rescale skip of the
+// FA5090 page (sections 2.6 and 2.8: skip exactly when the max did not
+// change); tau = 8 is FA4's lazy rescale that the same page describes in
+// section 3 (p stays <= 2^8, and the final division by l, accumulated
+// against the same m, makes the result exact either way).
 //
 // Causal (bottom-right): key tiles past the last row's diagonal are never
-// loaded or computed; only tiles that cross the diagonal (or the ragged end
-// of the keys) are masked (FA5090 page section 2.8, diagonal-only masking;
-// section 2.7 causal block skip).  CTAs are ordered heaviest-first (LPT,
+// loaded or computed (FA5090 section 2.7, causal block skip); only tiles that
+// cross the diagonal (or the ragged end of the keys) are masked (section
+// 2.8, diagonal-only masking).  CTAs are ordered heaviest-first (LPT,
 // section 2.7).
 //
 // Every mbarrier wait is bounded by a watchdog; a wait that runs out sets a
@@ -57,26 +61,23 @@ template <int D>
 struct PrefillLayout {
   static_assert(D == 64 || D == 128, "head dim");
   static constexpr int kQBytes = kBM * D * 2;    // one stage of Q
-  static constexpr int kPBytes = kBM * kBN * 2;  // one stage of P
   static constexpr int kKVBytes = kBN * D * 2;   // one K or V tile
   static constexpr int kBox = 128 * 64 * 2;      // one TMA box (64 cols)
-  static constexpr int kSlots = D == 128 ? 3 : 8;
+  static constexpr int kSlots = D == 128 ? 5 : 11;
   static constexpr int kOffQ = 0;
-  static constexpr int kOffP = kOffQ + kStages * kQBytes;
-  static constexpr int kOffKV = kOffP + kStages * kPBytes;
+  static constexpr int kOffKV = kOffQ + kStages * kQBytes;
   static constexpr int kOffMisc = kOffKV + kSlots * kKVBytes;
   // mbarrier indices
   static constexpr int Q_FULL = 0;    // [2]
   static constexpr int S_FULL = 2;    // [2]
-  static constexpr int S_FREE = 4;    // [2]
-  static constexpr int P_FULL = 6;    // [2]
-  static constexpr int A_READY = 8;   // [2]
-  static constexpr int O_READY = 10;  // [2]
-  static constexpr int O_FIXED = 12;  // [2]
-  static constexpr int DRAIN = 14;
-  static constexpr int KV_FULL = 15;            // [kSlots]
-  static constexpr int KV_EMPTY = 15 + kSlots;  // [kSlots]
-  static constexpr int kNumBars = 15 + 2 * kSlots;
+  static constexpr int P_FULL = 4;    // [2]
+  static constexpr int A_READY = 6;   // [2]
+  static constexpr int O_READY = 8;   // [2]
+  static constexpr int O_FIXED = 10;  // [2]
+  static constexpr int DRAIN = 12;
+  static constexpr int KV_FULL = 13;            // [kSlots]
+  static constexpr int KV_EMPTY = 13 + kSlots;  // [kSlots]
+  static constexpr int kNumBars = 13 + 2 * kSlots;
   static constexpr int kOffBars = kOffMisc;
   static constexpr int kOffAlpha = kOffBars + ((kNumBars * 8 + 15) / 16) * 16;
   static constexpr int kOffTmemSlot = kOffAlpha + kStages * kBM * 4;
@@ -103,15 +104,22 @@ struct Ctl {
   unsigned long long timeout;
 };
 
+// try_wait suspends the thread for a while before it reports "not yet", so
+// the abort flag and the clock are checked only every 8th round.
 __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, Ctl c) {
-  const uint64_t t0 = globaltimer_ns();
-  for (;;) {
+  uint64_t t0 = 0;
+  for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (*c.abort) return false;
-    if (globaltimer_ns() - t0 > c.timeout) {
-      *c.abort = 1u;
-      atomicExch(c.status, kStatusTimeout);
-      return false;
+    if ((n & 7u) == 0) {
+      if (*c.abort) return false;
+      const uint64_t t = globaltimer_ns();
+      if (t0 == 0) {
+        t0 = t;
+      } else if (t - t0 > c.timeout) {
+        *c.abort = 1u;
+        atomicExch(c.status, kStatusTimeout);
+        return false;
+      }
     }
   }
 }
@@ -131,7 +139,7 @@ __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity,
 
 // Wait used while draining after an abort: time-bounded only.
 __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity,
-                                        unsigned long long timeout) {
+                                           unsigned long long timeout) {
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
     if (globaltimer_ns() - t0 > timeout) return;
@@ -180,7 +188,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sQ = sbase + L::kOffQ;
-  const uint32_t sP = sbase + L::kOffP;
   const uint32_t sKV = sbase + L::kOffKV;
   const uint32_t bars = sbase + L::kOffBars;
   float* alpha_smem = reinterpret_cast<float*>(smem + L::kOffAlpha);
@@ -208,11 +215,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- setup ----
   if (threadIdx.x == 0) {
-    mbar_init(bar(L::Q_FULL + 0), 1);
-    mbar_init(bar(L::Q_FULL + 1), 1);
     for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(L::Q_FULL + s), 1);
       mbar_init(bar(L::S_FULL + s), 1);
-      mbar_init(bar(L::S_FREE + s), 4);
       mbar_init(bar(L::P_FULL + s), 4);
       mbar_init(bar(L::A_READY + s), 4);
       mbar_init(bar(L::O_READY + s), 1);
@@ -261,9 +266,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t t_lane = static_cast<uint32_t>(rq * 32) << 16;
     const uint32_t tS = tmem + t_lane + static_cast<uint32_t>(s * kBN);
     const uint32_t tO = tmem + t_lane + static_cast<uint32_t>(L::kTmemO + s * D);
-    const uint32_t pbuf = sP + static_cast<uint32_t>(s * L::kPBytes);
     const float c = p.scale_log2;
-    float m = -INFINITY;  // running max of c*s (log2 units)
+    const float tau = p.rescale_tau;
+    float m = -INFINITY;  // reference max of c*s (log2 units)
     float l = 0.f;        // running sum of 2^(c*s - m)
     bool ok = true;
 
@@ -277,9 +282,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld();
 #pragma unroll
       for (int cc = 0; cc < 8; ++cc) reg_fence16(sr[cc]);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::S_FREE + s));
 
       // mask: ragged key tail, and the causal diagonal
       const int key0 = j * kBN;
@@ -304,10 +306,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           mx2 = fmaxf(mx2, __uint_as_float(sr[cc][e + 2]));
           mx3 = fmaxf(mx3, __uint_as_float(sr[cc][e + 3]));
         }
-      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
-      const float m_new = fmaxf(m, mx * c);
+      const float t_max = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+      // raise the reference max only past the threshold (m = -inf: always)
+      const float m_new = t_max > m + tau ? t_max : m;
       const float m_use = m_new == -INFINITY ? 0.f : m_new;
-      const float alpha = ex2_approx(m - m_use);
+      const float alpha = m_new == m ? 1.f : ex2_approx(m - m_use);
       if (j > 0) {
         alpha_smem[s * kBM + r] = alpha;
         __syncwarp();
@@ -332,24 +335,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       l = l * alpha + ((l0 + l1) + (l2 + l3));
       m = m_new;
 
-      // P_s(j-1) must have been consumed by PV_s(j-1) before it is replaced
-      if (j > 0 && !wait_bar_warp(bar(L::O_READY + s), (j - 1) & 1, ctl)) {
-        ok = false;
-        break;
-      }
-      // 16 chunks of 8 keys; chunk q lives in 64-key half q/8, swizzled
+      // P_s (16-bit pairs) over the first 64 columns of S_s; every S value of
+      // this row is already in registers
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const int cc = q >> 1, e0 = (q & 1) * 8;
-        const uint32_t w0 = pack2<BF16>(__uint_as_float(sr[cc][e0 + 0]), __uint_as_float(sr[cc][e0 + 1]));
-        const uint32_t w1 = pack2<BF16>(__uint_as_float(sr[cc][e0 + 2]), __uint_as_float(sr[cc][e0 + 3]));
-        const uint32_t w2 = pack2<BF16>(__uint_as_float(sr[cc][e0 + 4]), __uint_as_float(sr[cc][e0 + 5]));
-        const uint32_t w3 = pack2<BF16>(__uint_as_float(sr[cc][e0 + 6]), __uint_as_float(sr[cc][e0 + 7]));
-        const uint32_t addr = pbuf + static_cast<uint32_t>((q >> 3) * L::kBox + r * 128 +
-                                                           (((q & 7) ^ (r & 7)) << 4));
-        st_shared_v4(addr, w0, w1, w2, w3);
+      for (int h = 0; h < 4; ++h) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int col = h * 32 + 2 * e;  // first key of the pair
+          pk[e] = pack2<BF16>(__uint_as_float(sr[col >> 4][col & 15]),
+                              __uint_as_float(sr[col >> 4][(col & 15) + 1]));
+        }
+        tmem_st16(tS + h * 16, pk);
       }
-      fence_proxy_async_smem();
+      tmem_wait_st();
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(L::P_FULL + s));
     }
@@ -426,14 +426,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (p.always_rescale || __any_sync(0xffffffffu, alpha != 1.f)) {
           const uint32_t tO = tmem + t_lane + static_cast<uint32_t>(L::kTmemO + s * D);
 #pragma unroll 1
-          for (int cc = 0; cc < D / 16; ++cc) {
-            uint32_t v[16];
-            tmem_ld16(tO + cc * 16, v);
+          for (int cc = 0; cc < D / 16; cc += 2) {
+            uint32_t v0[16], v1[16];
+            tmem_ld16(tO + cc * 16, v0);
+            tmem_ld16(tO + cc * 16 + 16, v1);
             tmem_wait_ld();
-            reg_fence16(v);
+            reg_fence16(v0);
+            reg_fence16(v1);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-            tmem_st16(tO + cc * 16, v);
+            for (int e = 0; e < 16; ++e) {
+              v0[e] = __float_as_uint(__uint_as_float(v0[e]) * alpha);
+              v1[e] = __float_as_uint(__uint_as_float(v1[e]) * alpha);
+            }
+            tmem_st16(tO + cc * 16, v0);
+            tmem_st16(tO + cc * 16 + 16, v1);
           }
           tmem_wait_st();
         }
@@ -462,11 +468,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                       smem_desc_sw128(kbuf + koff, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
         }
       };
-      auto issue_pv = [&](uint32_t d_tmem, uint32_t pbuf, uint32_t vbuf, bool acc) {
+      // A = P_s from tensor memory (8 columns per 16 keys), B = V (MN-major)
+      auto issue_pv = [&](uint32_t d_tmem, uint32_t p_tmem, uint32_t vbuf, bool acc) {
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint32_t poff = static_cast<uint32_t>((kk >> 2) * L::kBox + (kk & 3) * 32);
-          umma_f16_ss(d_tmem, smem_desc_sw128(pbuf + poff, 16, 1024),
+          umma_f16_ts(d_tmem, p_tmem + static_cast<uint32_t>(kk * 8),
                       smem_desc_sw128(vbuf + static_cast<uint32_t>(kk * 16 * 128), L::kBox, 1024),
                       kIdescPV, (acc || kk > 0) ? 1u : 0u);
         }
@@ -479,8 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int fk = 2 * j, fv_prev = 2 * (j - 1) + 1, fv = 2 * j + 1;
         if (j < n_kv) {
           if (!wait_bar(bar(L::KV_FULL + slot_of(fk)), par_of(fk), ctl)) { ok = false; break; }
-          if (j < nT0) {
-            if (j > 0 && !wait_bar(bar(L::S_FREE + 0), (j - 1) & 1, ctl)) { ok = false; break; }
+          if (j < nT0) {  // QK_0(j): overwrites P_0(j-1), whose PV was issued before
             tc_fence_after();
             issue_qk(tS0, sQ, sKV + slot_of(fk) * L::kKVBytes);
             umma_commit(bar(L::S_FULL + 0));
@@ -495,13 +500,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          issue_pv(tO1, sP + L::kPBytes, sKV + slot_of(fv_prev) * L::kKVBytes, j - 1 > 0);
+          issue_pv(tO1, tS1, sKV + slot_of(fv_prev) * L::kKVBytes, j - 1 > 0);
           umma_commit(bar(L::O_READY + 1));
           umma_commit(bar(L::KV_EMPTY + slot_of(fv_prev)));
           issued = true;
         }
-        if (j < n_kv) {
-          if (j > 0 && !wait_bar(bar(L::S_FREE + 1), (j - 1) & 1, ctl)) { ok = false; break; }
+        if (j < n_kv) {  // QK_1(j): overwrites P_1(j-1), whose PV was issued above
           tc_fence_after();
           issue_qk(tS1, sQ + L::kQBytes, sKV + slot_of(fk) * L::kKVBytes);
           umma_commit(bar(L::S_FULL + 1));
@@ -515,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             tc_fence_after();
-            issue_pv(tO0, sP, sKV + slot_of(fv) * L::kKVBytes, j > 0);
+            issue_pv(tO0, tS0, sKV + slot_of(fv) * L::kKVBytes, j > 0);
             umma_commit(bar(L::O_READY + 0));
           }
         }
@@ -562,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // drain: every load issued lands before shared memory goes away
       wait_drain(bar(L::Q_FULL + 0), 0, p.timeout_ns);
       wait_drain(bar(L::Q_FULL + 1), 0, p.timeout_ns);
-#pragma unroll
+#pragma unroll 1
       for (int i = 0; i < L::kSlots; ++i)
         if (last_fill[i] >= 0)
           wait_drain(bar(L::KV_FULL + i), static_cast<uint32_t>((last_fill[i] / L::kSlots) & 1),

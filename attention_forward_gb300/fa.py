@@ -21,6 +21,7 @@ FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED = 0, 1, 2
 FA_ERR_CUDA, FA_ERR_WORKSPACE, FA_ERR_TIMEOUT = 3, 4, 5
 FA_FLAG_NO_LPT = 0x1
 FA_FLAG_ALWAYS_RESCALE = 0x2
+FA_FLAG_EXACT_MAX = 0x4
 FA_FLAG_TEST_STALL = 0x100
 
 _DTYPE = {torch.float16: FA_F16, torch.bfloat16: FA_BF16}

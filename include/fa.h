@@ -67,6 +67,13 @@ typedef enum {
 #define FA_FLAG_ALWAYS_RESCALE 0x2u  /* rescale O on every key tile, not only
                                         when the row max changes (bitwise
                                         identical either way)              */
+#define FA_FLAG_EXACT_MAX 0x4u       /* prefill: carry the exact running row
+                                        max (rescale O whenever it grows)
+                                        instead of raising the reference max
+                                        only when a tile's max exceeds it by
+                                        more than 8 in log2 units; both are
+                                        exact after the final division by
+                                        the row sum                         */
 #define FA_FLAG_TEST_STALL 0x100u    /* test hook: the K/V producer withholds
                                         its second tile, so the consumers'
                                         bounded waits run out and the kernel

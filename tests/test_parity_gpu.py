@@ -106,6 +106,19 @@ def test_repeat_lpt_and_rescale_switches_are_bitwise_identical():
         assert torch.equal(o, o1) and torch.equal(l, l1)
 
 
+@pytest.mark.parametrize("w", [inputs.C2_X4, inputs.C2_X4_CAUSAL, inputs.PR1],
+                         ids=lambda w: w.name)
+def test_exact_running_max_mode(w):
+    """FA_FLAG_EXACT_MAX (rescale whenever the row max grows) passes the gate
+    too, and switching the rescale off when alpha == 1 changes no bit."""
+    q, k, v = w.make()
+    o1, l1 = run_kernel(q, k, v, w.causal, flags=fa.FA_FLAG_EXACT_MAX)
+    _assert(check(q, k, v, o1, l1, w.causal, w.dtype))
+    o2, l2 = run_kernel(q, k, v, w.causal,
+                        flags=fa.FA_FLAG_EXACT_MAX | fa.FA_FLAG_ALWAYS_RESCALE)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
 def test_concurrent_streams_bitwise_identical():
     q, k, v = inputs.make_qkv(2, 8, 1024, 1024, 128, "bf16", 6)
     dq, dk, dv = (t.cuda() for t in (q, k, v))
