@@ -7,7 +7,7 @@
 //   warps 0-3   softmax, stage 0   one thread per query row (TMEM lane)
 //   warps 4-7   softmax, stage 1
 //   warps 8-11  correction: rescales O in TMEM when a row's reference max moved
-//   warp  12    tcgen05.mma issuer (one thread) + TMEM allocation
+//   warp  12    tcgen05.mma issue (whole warp, one elected lane) + TMEM alloc
 //   warp  13    TMA producer (one thread): Q once, then K/V tiles
 //   warps 14-15 idle (they complete the fourth warpgroup)
 //
@@ -15,8 +15,8 @@
 // (fp32), O_s at 256 + s*D (fp32).  Softmax writes P_s as packed 16-bit
 // pairs over the first 64 columns of S_s, and PV reads its A operand from
 // there (P never touches shared memory).  The next S_s overwrites P_s; the
-// single MMA thread issues PV_s(j) before QK_s(j+1) and the tensor core
-// executes one thread's MMAs in issue order.
+// MMA warp's elected lane issues PV_s(j) before QK_s(j+1) and the tensor
+// core executes one thread's MMAs in issue order.
 //
 // Issue order of the tensor core, per key tile j:
 //     QK_0(j)  PV_1(j-1)  QK_1(j)  PV_0(j)
@@ -452,13 +452,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 12) {
     // ============================== MMA issuer ==============================
-    if (lane == 0) {
+    // the whole warp runs this loop in lockstep; each MMA / commit wrapper
+    // elects the issuing lane itself
+    {
       constexpr uint32_t kIdescQK = idesc_f16(BF16, false, false, kBM, kBN);
       constexpr uint32_t kIdescPV = idesc_f16(BF16, false, true, kBM, D);
       const uint32_t tS0 = tmem, tS1 = tmem + kBN;
       const uint32_t tO0 = tmem + L::kTmemO, tO1 = tmem + L::kTmemO + D;
       bool issued = false;
-      bool ok = wait_bar(bar(L::Q_FULL + 0), 0, ctl) && wait_bar(bar(L::Q_FULL + 1), 0, ctl);
+      bool ok = wait_bar_warp(bar(L::Q_FULL + 0), 0, ctl) &&
+                wait_bar_warp(bar(L::Q_FULL + 1), 0, ctl);
 
       auto issue_qk = [&](uint32_t d_tmem, uint32_t qbuf, uint32_t kbuf) {
 #pragma unroll
@@ -484,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; ok && j <= n_kv; ++j) {
         const int fk = 2 * j, fv_prev = 2 * (j - 1) + 1, fv = 2 * j + 1;
         if (j < n_kv) {
-          if (!wait_bar(bar(L::KV_FULL + slot_of(fk)), par_of(fk), ctl)) { ok = false; break; }
+          if (!wait_bar_warp(bar(L::KV_FULL + slot_of(fk)), par_of(fk), ctl)) { ok = false; break; }
           if (j < nT0) {  // QK_0(j): overwrites P_0(j-1), whose PV was issued before
             tc_fence_after();
             issue_qk(tS0, sQ, sKV + slot_of(fk) * L::kKVBytes);
@@ -493,9 +496,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (j >= 1 && j - 1 < nT1) {  // PV_1(j-1)
-          if (!wait_bar(bar(L::KV_FULL + slot_of(fv_prev)), par_of(fv_prev), ctl) ||
-              !wait_bar(bar(L::P_FULL + 1), (j - 1) & 1, ctl) ||
-              (j - 1 >= 1 && !wait_bar(bar(L::O_FIXED + 1), (j - 2) & 1, ctl))) {
+          if (!wait_bar_warp(bar(L::KV_FULL + slot_of(fv_prev)), par_of(fv_prev), ctl) ||
+              !wait_bar_warp(bar(L::P_FULL + 1), (j - 1) & 1, ctl) ||
+              (j - 1 >= 1 && !wait_bar_warp(bar(L::O_FIXED + 1), (j - 2) & 1, ctl))) {
             ok = false;
             break;
           }
@@ -512,9 +515,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_commit(bar(L::KV_EMPTY + slot_of(fk)));
           issued = true;
           if (j < nT0) {  // PV_0(j)
-            if (!wait_bar(bar(L::KV_FULL + slot_of(fv)), par_of(fv), ctl) ||
-                !wait_bar(bar(L::P_FULL + 0), j & 1, ctl) ||
-                (j >= 1 && !wait_bar(bar(L::O_FIXED + 0), (j - 1) & 1, ctl))) {
+            if (!wait_bar_warp(bar(L::KV_FULL + slot_of(fv)), par_of(fv), ctl) ||
+                !wait_bar_warp(bar(L::P_FULL + 0), j & 1, ctl) ||
+                (j >= 1 && !wait_bar_warp(bar(L::O_FIXED + 0), (j - 1) & 1, ctl))) {
               ok = false;
               break;
             }

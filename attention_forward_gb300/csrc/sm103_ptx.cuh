@@ -167,15 +167,23 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+// The MMA and commit wrappers below are executed by a whole, converged warp:
+// elect.sync inside the asm picks the one lane that issues, so the operand
+// descriptors, computed identically by every lane, stay warp-uniform.  A
+// single divergent lane issuing tcgen05.mma measured ~100 cycles per
+// instruction on GB300; the converged form issues faster than the tensor
+// core consumes (64 cycles per 128x128x16).
+
 // D[tmem] (+)= A[smem desc] * B[smem desc], kind::f16 (fp16/bf16 in, fp32
-// accumulate), issued by one thread.
+// accumulate).
 __device__ __forceinline__ void umma_f16_ss(uint32_t d_tmem, uint64_t a_desc,
                                             uint64_t b_desc, uint32_t idesc,
                                             uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
           d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
@@ -187,20 +195,23 @@ __device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem,
                                             uint64_t b_desc, uint32_t idesc,
                                             uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(
           d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
-// Arrive once on `bar` when every tcgen05 op issued so far by this thread
-// has completed.
+// Arrive once on `bar` when every tcgen05 op issued so far by the elected
+// lane has completed (the same lane elect.sync picks for the MMAs).
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 "
-      "[%0];" ::"r"(bar)
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 "
+      "[%0];\n\t}" ::"r"(bar)
       : "memory");
 }
 
