@@ -70,14 +70,13 @@ struct PrefillLayout {
   // mbarrier indices
   static constexpr int Q_FULL = 0;    // [2]
   static constexpr int S_FULL = 2;    // [2]
-  static constexpr int P_FULL = 4;    // [2]
+  static constexpr int PV_READY = 4;  // [2] P stored and O rescaled
   static constexpr int A_READY = 6;   // [2]
   static constexpr int O_READY = 8;   // [2]
-  static constexpr int O_FIXED = 10;  // [2]
-  static constexpr int DRAIN = 12;
-  static constexpr int KV_FULL = 13;            // [kSlots]
-  static constexpr int KV_EMPTY = 13 + kSlots;  // [kSlots]
-  static constexpr int kNumBars = 13 + 2 * kSlots;
+  static constexpr int DRAIN = 10;
+  static constexpr int KV_FULL = 11;            // [kSlots]
+  static constexpr int KV_EMPTY = 11 + kSlots;  // [kSlots]
+  static constexpr int kNumBars = 11 + 2 * kSlots;
   static constexpr int kOffBars = kOffMisc;
   static constexpr int kOffAlpha = kOffBars + ((kNumBars * 8 + 15) / 16) * 16;
   static constexpr int kOffTmemSlot = kOffAlpha + kStages * kBM * 4;
@@ -218,10 +217,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(L::Q_FULL + s), 1);
       mbar_init(bar(L::S_FULL + s), 1);
-      mbar_init(bar(L::P_FULL + s), 4);
+      mbar_init(bar(L::PV_READY + s), 8);  // 4 softmax warps + 4 correction warps
       mbar_init(bar(L::A_READY + s), 4);
       mbar_init(bar(L::O_READY + s), 1);
-      mbar_init(bar(L::O_FIXED + s), 4);
     }
     mbar_init(bar(L::DRAIN), 1);
     for (int i = 0; i < L::kSlots; ++i) {
@@ -300,11 +298,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int cc = 0; cc < 8; ++cc)
 #pragma unroll
-        for (int e = 0; e < 16; e += 4) {
-          mx0 = fmaxf(mx0, __uint_as_float(sr[cc][e + 0]));
-          mx1 = fmaxf(mx1, __uint_as_float(sr[cc][e + 1]));
-          mx2 = fmaxf(mx2, __uint_as_float(sr[cc][e + 2]));
-          mx3 = fmaxf(mx3, __uint_as_float(sr[cc][e + 3]));
+        for (int e = 0; e < 16; e += 8) {
+          mx0 = fmax3(mx0, __uint_as_float(sr[cc][e + 0]), __uint_as_float(sr[cc][e + 1]));
+          mx1 = fmax3(mx1, __uint_as_float(sr[cc][e + 2]), __uint_as_float(sr[cc][e + 3]));
+          mx2 = fmax3(mx2, __uint_as_float(sr[cc][e + 4]), __uint_as_float(sr[cc][e + 5]));
+          mx3 = fmax3(mx3, __uint_as_float(sr[cc][e + 6]), __uint_as_float(sr[cc][e + 7]));
         }
       const float t_max = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
       // raise the reference max only past the threshold (m = -inf: always)
@@ -317,16 +315,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(bar(L::A_READY + s));
       }
       const float neg_m = -m_use;
+      // p = 2^(s*c - m): the argument as packed fp32x2 FMAs, the row sum as
+      // packed fp32x2 adds (two columns per instruction)
       float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
 #pragma unroll
       for (int cc = 0; cc < 8; ++cc)
 #pragma unroll
         for (int e = 0; e < 16; e += 4) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[cc][e + 0]), c, neg_m));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[cc][e + 1]), c, neg_m));
-          const float p2 = ex2_approx(fmaf(__uint_as_float(sr[cc][e + 2]), c, neg_m));
-          const float p3 = ex2_approx(fmaf(__uint_as_float(sr[cc][e + 3]), c, neg_m));
-          l0 += p0; l1 += p1; l2 += p2; l3 += p3;
+          float x0, x1, x2, x3;
+          ffma2(x0, x1, __uint_as_float(sr[cc][e + 0]), __uint_as_float(sr[cc][e + 1]), c, c,
+                neg_m, neg_m);
+          ffma2(x2, x3, __uint_as_float(sr[cc][e + 2]), __uint_as_float(sr[cc][e + 3]), c, c,
+                neg_m, neg_m);
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+          fadd2(l0, l1, l0, l1, p0, p1);
+          fadd2(l2, l3, l2, l3, p2, p3);
           sr[cc][e + 0] = __float_as_uint(p0);
           sr[cc][e + 1] = __float_as_uint(p1);
           sr[cc][e + 2] = __float_as_uint(p2);
@@ -351,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::P_FULL + s));
+      if (lane == 0) mbar_arrive(bar(L::PV_READY + s));
     }
 
     // ------------------------------ epilogue ------------------------------
@@ -410,42 +414,49 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (wg == 2) {
     // ============================== correction ==============================
+    // For every key tile j of stage s: once softmax has published alpha and
+    // PV_s(j-1) has completed, rescale O_s if any row of this warp moved its
+    // reference max, then arrive on PV_READY_s (together with the softmax
+    // warps' arrival after storing P, that releases PV_s(j)).  Tile 0 has no
+    // O to rescale and only arrives.
     const int rq = warp & 3;
     const int r = rq * 32 + lane;
     const uint32_t t_lane = static_cast<uint32_t>(rq * 32) << 16;
 #pragma unroll 1
-    for (int j = 1; j < n_kv; ++j) {
+    for (int j = 0; j < n_kv; ++j) {
       bool ok = true;
 #pragma unroll 1
       for (int s = 0; s < 2; ++s) {
         if (j >= (s == 0 ? nT0 : nT1)) continue;
-        if (!wait_bar_warp(bar(L::A_READY + s), (j - 1) & 1, ctl)) { ok = false; break; }
-        const float alpha = alpha_smem[s * kBM + r];
-        if (!wait_bar_warp(bar(L::O_READY + s), (j - 1) & 1, ctl)) { ok = false; break; }
-        tc_fence_after();
-        if (p.always_rescale || __any_sync(0xffffffffu, alpha != 1.f)) {
-          const uint32_t tO = tmem + t_lane + static_cast<uint32_t>(L::kTmemO + s * D);
+        if (j > 0) {
+          if (!wait_bar_warp(bar(L::A_READY + s), (j - 1) & 1, ctl)) { ok = false; break; }
+          const float alpha = alpha_smem[s * kBM + r];
+          if (!wait_bar_warp(bar(L::O_READY + s), (j - 1) & 1, ctl)) { ok = false; break; }
+          tc_fence_after();
+          if (p.always_rescale || __any_sync(0xffffffffu, alpha != 1.f)) {
+            const uint32_t tO = tmem + t_lane + static_cast<uint32_t>(L::kTmemO + s * D);
 #pragma unroll 1
-          for (int cc = 0; cc < D / 16; cc += 2) {
-            uint32_t v0[16], v1[16];
-            tmem_ld16(tO + cc * 16, v0);
-            tmem_ld16(tO + cc * 16 + 16, v1);
-            tmem_wait_ld();
-            reg_fence16(v0);
-            reg_fence16(v1);
+            for (int cc = 0; cc < D / 16; cc += 2) {
+              uint32_t v0[16], v1[16];
+              tmem_ld16(tO + cc * 16, v0);
+              tmem_ld16(tO + cc * 16 + 16, v1);
+              tmem_wait_ld();
+              reg_fence16(v0);
+              reg_fence16(v1);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              v0[e] = __float_as_uint(__uint_as_float(v0[e]) * alpha);
-              v1[e] = __float_as_uint(__uint_as_float(v1[e]) * alpha);
+              for (int e = 0; e < 16; ++e) {
+                v0[e] = __float_as_uint(__uint_as_float(v0[e]) * alpha);
+                v1[e] = __float_as_uint(__uint_as_float(v1[e]) * alpha);
+              }
+              tmem_st16(tO + cc * 16, v0);
+              tmem_st16(tO + cc * 16 + 16, v1);
             }
-            tmem_st16(tO + cc * 16, v0);
-            tmem_st16(tO + cc * 16 + 16, v1);
+            tmem_wait_st();
           }
-          tmem_wait_st();
+          tc_fence_before();
         }
-        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(L::O_FIXED + s));
+        if (lane == 0) mbar_arrive(bar(L::PV_READY + s));
       }
       if (!ok) break;
     }
@@ -495,10 +506,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             issued = true;
           }
         }
-        if (j >= 1 && j - 1 < nT1) {  // PV_1(j-1)
-          if (!wait_bar_warp(bar(L::KV_FULL + slot_of(fv_prev)), par_of(fv_prev), ctl) ||
-              !wait_bar_warp(bar(L::P_FULL + 1), (j - 1) & 1, ctl) ||
-              (j - 1 >= 1 && !wait_bar_warp(bar(L::O_FIXED + 1), (j - 2) & 1, ctl))) {
+        if (j >= 1 && j - 1 < nT1) {  // PV_1(j-1); V_(j-1) was waited for by PV_0(j-1)
+          if ((j - 1 >= nT0 &&
+               !wait_bar_warp(bar(L::KV_FULL + slot_of(fv_prev)), par_of(fv_prev), ctl)) ||
+              !wait_bar_warp(bar(L::PV_READY + 1), (j - 1) & 1, ctl)) {
             ok = false;
             break;
           }
@@ -516,8 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           issued = true;
           if (j < nT0) {  // PV_0(j)
             if (!wait_bar_warp(bar(L::KV_FULL + slot_of(fv)), par_of(fv), ctl) ||
-                !wait_bar_warp(bar(L::P_FULL + 0), j & 1, ctl) ||
-                (j >= 1 && !wait_bar_warp(bar(L::O_FIXED + 0), (j - 1) & 1, ctl))) {
+                !wait_bar_warp(bar(L::PV_READY + 0), j & 1, ctl)) {
               ok = false;
               break;
             }

@@ -101,6 +101,16 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* desc,
       : "memory");
 }
 
+// Prefetch a 3-D tile into L2 (no shared memory, no completion signal).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const void* desc, int32_t x,
+                                                   int32_t y, int32_t z) {
+  asm volatile(
+      "cp.async.bulk.prefetch.tensor.3d.L2.global [%0, {%1, %2, %3}];" ::"l"(
+          reinterpret_cast<uint64_t>(desc)),
+      "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
 // 3-D tiled store shared -> global (bulk-group completion).
 __device__ __forceinline__ void tma_store_3d(const void* desc, uint32_t src,
                                              int32_t x, int32_t y, int32_t z) {
@@ -269,6 +279,34 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// max(a, b, c) in one instruction (sm_100 family three-input max).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Packed pair of fp32 fused multiply-adds (one fma.rn.f32x2):
+// (d0, d1) = (a0 * b0 + c0, a1 * b1 + c1).
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1,
+                                      float b0, float b1, float c0, float c1) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
+// Packed pair of fp32 additions (one add.rn.f32x2).
+__device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1,
+                                      float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
 // ------------------------------------------------------------ descriptors
