@@ -474,22 +474,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = wait_bar_warp(bar(L::Q_FULL + 0), 0, ctl) &&
                 wait_bar_warp(bar(L::Q_FULL + 1), 0, ctl);
 
+      // one asm block per GEMM: K = D for QK (both operands K-major in
+      // smem), K = 128 keys for PV (A = P_s from tensor memory, B = V MN-major)
       auto issue_qk = [&](uint32_t d_tmem, uint32_t qbuf, uint32_t kbuf) {
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = static_cast<uint32_t>((kk >> 2) * L::kBox + (kk & 3) * 32);
-          umma_f16_ss(d_tmem, smem_desc_sw128(qbuf + koff, 16, 1024),
-                      smem_desc_sw128(kbuf + koff, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
+        const uint64_t da = smem_desc_sw128(qbuf, 16, 1024);
+        const uint64_t db = smem_desc_sw128(kbuf, 16, 1024);
+        if constexpr (D == 128) {
+          umma_f16_ss_k128(d_tmem, da, db, kIdescQK, 0u);
+        } else {
+          umma_f16_ss_k64(d_tmem, da, db, kIdescQK, 0u);
         }
       };
-      // A = P_s from tensor memory (8 columns per 16 keys), B = V (MN-major)
       auto issue_pv = [&](uint32_t d_tmem, uint32_t p_tmem, uint32_t vbuf, bool acc) {
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          umma_f16_ts(d_tmem, p_tmem + static_cast<uint32_t>(kk * 8),
-                      smem_desc_sw128(vbuf + static_cast<uint32_t>(kk * 16 * 128), L::kBox, 1024),
-                      kIdescPV, (acc || kk > 0) ? 1u : 0u);
-        }
+        umma_f16_ts_k128(d_tmem, p_tmem, smem_desc_sw128(vbuf, L::kBox, 1024), kIdescPV,
+                         acc ? 1u : 0u);
       };
       auto slot_of = [&](int fill) { return fill % L::kSlots; };
       auto par_of = [&](int fill) { return static_cast<uint32_t>((fill / L::kSlots) & 1); };

@@ -214,6 +214,94 @@ __device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem,
       : "memory");
 }
 
+// Eight K=16 steps of D (+)= A * B with both operands K-major, 128-byte
+// swizzled, in shared memory: the K = 128 contraction of a 64-column-box
+// pair.  Step k reads 32 bytes further into each 128-byte row (descriptor
+// start + 2 in 16-byte units) for k = 0..3, then the second 64-column box
+// (+16384 bytes = +1024 units).  One elect.sync for the whole group; the
+// first step overwrites D unless `accumulate`.
+__device__ __forceinline__ void umma_f16_ss_k128(uint32_t d_tmem, uint64_t a_desc,
+                                                 uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e, t;\n\t"
+      ".reg .b64 a1, a2, a3, a4, a5, a6, a7, b1, b2, b3, b4, b5, b6, b7;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 t, 0, 0;\n\t"
+      "add.s64 a1, %1, 2;\n\t add.s64 b1, %2, 2;\n\t"
+      "add.s64 a2, %1, 4;\n\t add.s64 b2, %2, 4;\n\t"
+      "add.s64 a3, %1, 6;\n\t add.s64 b3, %2, 6;\n\t"
+      "add.s64 a4, %1, 1024;\n\t add.s64 b4, %2, 1024;\n\t"
+      "add.s64 a5, %1, 1026;\n\t add.s64 b5, %2, 1026;\n\t"
+      "add.s64 a6, %1, 1028;\n\t add.s64 b6, %2, 1028;\n\t"
+      "add.s64 a7, %1, 1030;\n\t add.s64 b7, %2, 1030;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a4, b4, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a5, b5, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a6, b6, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a7, b7, %3, t;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Four K=16 steps of D (+)= A * B for a K = 64 contraction (one 64-column
+// box): K-major, 128-byte swizzled operands in shared memory.
+__device__ __forceinline__ void umma_f16_ss_k64(uint32_t d_tmem, uint64_t a_desc,
+                                                uint64_t b_desc, uint32_t idesc,
+                                                uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e, t;\n\t"
+      ".reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 t, 0, 0;\n\t"
+      "add.s64 a1, %1, 2;\n\t add.s64 b1, %2, 2;\n\t"
+      "add.s64 a2, %1, 4;\n\t add.s64 b2, %2, 4;\n\t"
+      "add.s64 a3, %1, 6;\n\t add.s64 b3, %2, 6;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %3, t;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Eight K=16 steps of D (+)= A * B with A (128 rows x 128 K of 16-bit pairs)
+// in tensor memory, 8 columns per step, and B MN-major 128-byte swizzled in
+// shared memory, 16 K rows (2048 bytes = 128 descriptor units) per step.
+__device__ __forceinline__ void umma_f16_ts_k128(uint32_t d_tmem, uint32_t a_tmem,
+                                                 uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e, t;\n\t"
+      ".reg .b32 a1, a2, a3, a4, a5, a6, a7;\n\t"
+      ".reg .b64 b1, b2, b3, b4, b5, b6, b7;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 t, 0, 0;\n\t"
+      "add.s32 a1, %1, 8;\n\t  add.s64 b1, %2, 128;\n\t"
+      "add.s32 a2, %1, 16;\n\t add.s64 b2, %2, 256;\n\t"
+      "add.s32 a3, %1, 24;\n\t add.s64 b3, %2, 384;\n\t"
+      "add.s32 a4, %1, 32;\n\t add.s64 b4, %2, 512;\n\t"
+      "add.s32 a5, %1, 40;\n\t add.s64 b5, %2, 640;\n\t"
+      "add.s32 a6, %1, 48;\n\t add.s64 b6, %2, 768;\n\t"
+      "add.s32 a7, %1, 56;\n\t add.s64 b7, %2, 896;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a4], b4, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a5], b5, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a6], b6, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a7], b7, %3, t;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 op issued so far by the elected
 // lane has completed (the same lane elect.sync picks for the MMAs).
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
