@@ -137,8 +137,12 @@ LONG32K = Workload("long_B1H8S32768D128_bf16_causal", 1, 8, 32768, 32768, 128,
                    "bf16", True, 3)
 DECODE = Workload("decode_B32H32Sq1Skv8192D128_bf16", 32, 32, 1, 8192, 128,
                   "bf16", False, 4)
+# a decode case small enough for a multi-pass profiler capture (537 MB of K/V,
+# still larger than L2)
+DECODE_SMALL = Workload("decode_B4H32Sq1Skv8192D128_bf16", 4, 32, 1, 8192, 128,
+                        "bf16", False, 4, tags=("profile",))
 SWEEP = _sweep()
 
 ALL = (PR1, C2, C2_CAUSAL, C2_X4, C2_X4_CAUSAL, HEADLINE, LONG16K, LONG32K,
-       DECODE) + SWEEP
+       DECODE, DECODE_SMALL) + SWEEP
 BY_NAME = {w.name: w for w in ALL}
