@@ -55,6 +55,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-gemm-ceiling", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="--impl reference: total oracle time over all steps")
     return ap.parse_args(argv)
 
 
@@ -68,6 +70,13 @@ def dist_env():
 def shard_seed(seed: int, rank: int) -> int:
     """Each rank draws its own batch (weak scaling)."""
     return seed + 1000 * rank
+
+
+def job_throughput(flops_per_step: float, steps: int, world: int,
+                   max_seconds: float) -> float:
+    """Whole-job TFLOP/s: every rank ran `steps` steps of its own batch (weak
+    scaling), the job took as long as the slowest rank."""
+    return flops_per_step * steps * world / max_seconds / 1e12
 
 
 def max_over_ranks(x: float, world: int, device) -> float:
@@ -280,7 +289,7 @@ def bench_reference(args, w):
     # each step: a bounded row sample, sized so the whole run stays near a
     # couple of minutes
     smp = OracleSample(w)
-    per_step = min(10.0, max(0.02, 120.0 / max(1, args.steps + args.warmup)))
+    per_step = min(10.0, max(0.02, args.ref_seconds / max(1, args.steps + args.warmup)))
     n = smp.rows_for(per_step)
     for _ in range(args.warmup):
         smp.run(n)
@@ -369,7 +378,7 @@ def bench_ours(args, w):
     launch_s = statistics.mean(a.elapsed_time(b) for a, b in ev) / 1e3
     total_max = max_over_ranks(total_s, world, device)
     flops_step = w.flops()
-    value = flops_step * K * world / total_max / 1e12
+    value = job_throughput(flops_step, K, world, total_max)
 
     peaks, peak_src = load_peaks()
     if decode:
