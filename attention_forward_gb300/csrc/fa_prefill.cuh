@@ -315,43 +315,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(bar(L::A_READY + s));
       }
       const float neg_m = -m_use;
-      // p = 2^(s*c - m): the argument as packed fp32x2 FMAs, the row sum as
-      // packed fp32x2 adds (two columns per instruction)
+      // p = 2^(s*c - m) in four 32-column pieces: the argument as packed
+      // fp32x2 FMAs, the row sum as packed fp32x2 adds; each piece is packed
+      // to 16-bit pairs and stored over the first 64 columns of S_s (every S
+      // value of this row is already in registers) while the next piece's
+      // exponentials run
       float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
-#pragma unroll
-      for (int cc = 0; cc < 8; ++cc)
-#pragma unroll
-        for (int e = 0; e < 16; e += 4) {
-          float x0, x1, x2, x3;
-          ffma2(x0, x1, __uint_as_float(sr[cc][e + 0]), __uint_as_float(sr[cc][e + 1]), c, c,
-                neg_m, neg_m);
-          ffma2(x2, x3, __uint_as_float(sr[cc][e + 2]), __uint_as_float(sr[cc][e + 3]), c, c,
-                neg_m, neg_m);
-          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-          const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
-          fadd2(l0, l1, l0, l1, p0, p1);
-          fadd2(l2, l3, l2, l3, p2, p3);
-          sr[cc][e + 0] = __float_as_uint(p0);
-          sr[cc][e + 1] = __float_as_uint(p1);
-          sr[cc][e + 2] = __float_as_uint(p2);
-          sr[cc][e + 3] = __float_as_uint(p3);
-        }
-      l = l * alpha + ((l0 + l1) + (l2 + l3));
-      m = m_new;
-
-      // P_s (16-bit pairs) over the first 64 columns of S_s; every S value of
-      // this row is already in registers
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
         uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int col = h * 32 + 2 * e;  // first key of the pair
-          pk[e] = pack2<BF16>(__uint_as_float(sr[col >> 4][col & 15]),
-                              __uint_as_float(sr[col >> 4][(col & 15) + 1]));
+        for (int q = 0; q < 8; ++q) {
+          const int col = h * 32 + q * 4;
+          uint32_t* v = &sr[col >> 4][col & 15];
+          float x0, x1, x2, x3;
+          ffma2(x0, x1, __uint_as_float(v[0]), __uint_as_float(v[1]), c, c, neg_m, neg_m);
+          ffma2(x2, x3, __uint_as_float(v[2]), __uint_as_float(v[3]), c, c, neg_m, neg_m);
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+          fadd2(l0, l1, l0, l1, p0, p1);
+          fadd2(l2, l3, l2, l3, p2, p3);
+          pk[2 * q] = pack2<BF16>(p0, p1);
+          pk[2 * q + 1] = pack2<BF16>(p2, p3);
         }
         tmem_st16(tS + h * 16, pk);
       }
+      l = l * alpha + ((l0 + l1) + (l2 + l3));
+      m = m_new;
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
