@@ -18,8 +18,8 @@
 // MMA warp's elected lane issues PV_s(j) before QK_s(j+1) and the tensor
 // core executes one thread's MMAs in issue order.
 //
-// Issue order of the tensor core, per key tile j:
-//     QK_0(j)  PV_1(j-1)  QK_1(j)  PV_0(j)
+// Issue order of the tensor core: QK_0(0) QK_1(0), then per key tile j
+//     PV_0(j)  QK_0(j+1)  PV_1(j)  QK_1(j+1)
 // so that each softmax warpgroup has two GEMMs of the other stage to hide
 // behind (the aim of the ping-pong on the G5 page).  K and V occupy separate
 // slots of one ring with their own full/empty barriers (the decoupled K/V
@@ -482,47 +482,53 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto slot_of = [&](int fill) { return fill % L::kSlots; };
       auto par_of = [&](int fill) { return static_cast<uint32_t>((fill / L::kSlots) & 1); };
 
-#pragma unroll 1
-      for (int j = 0; ok && j <= n_kv; ++j) {
-        const int fk = 2 * j, fv_prev = 2 * (j - 1) + 1, fv = 2 * j + 1;
-        if (j < n_kv) {
-          if (!wait_bar_warp(bar(L::KV_FULL + slot_of(fk)), par_of(fk), ctl)) { ok = false; break; }
-          if (j < nT0) {  // QK_0(j): overwrites P_0(j-1), whose PV was issued before
-            tc_fence_after();
-            issue_qk(tS0, sQ, sKV + slot_of(fk) * L::kKVBytes);
+      // Tensor-core order: QK_0(0) QK_1(0), then per key tile j
+      //   PV_0(j) QK_0(j+1) PV_1(j) QK_1(j+1)
+      // Each QK_s(j+1) follows PV_s(j) at once (it overwrites P_s(j)); the
+      // wait for K_(j+1) is done earlier, while the softmax of tile j runs.
+      if (n_kv > 0) {
+        ok = wait_bar_warp(bar(L::KV_FULL + slot_of(0)), par_of(0), ctl);
+        if (ok) {
+          tc_fence_after();
+          if (nT0 > 0) {
+            issue_qk(tS0, sQ, sKV + slot_of(0) * L::kKVBytes);
             umma_commit(bar(L::S_FULL + 0));
-            issued = true;
           }
-        }
-        if (j >= 1 && j - 1 < nT1) {  // PV_1(j-1); V_(j-1) was waited for by PV_0(j-1)
-          if ((j - 1 >= nT0 &&
-               !wait_bar_warp(bar(L::KV_FULL + slot_of(fv_prev)), par_of(fv_prev), ctl)) ||
-              !wait_bar_warp(bar(L::PV_READY + 1), (j - 1) & 1, ctl)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          issue_pv(tO1, tS1, sKV + slot_of(fv_prev) * L::kKVBytes, j - 1 > 0);
-          umma_commit(bar(L::O_READY + 1));
-          umma_commit(bar(L::KV_EMPTY + slot_of(fv_prev)));
-          issued = true;
-        }
-        if (j < n_kv) {  // QK_1(j): overwrites P_1(j-1), whose PV was issued above
-          tc_fence_after();
-          issue_qk(tS1, sQ + L::kQBytes, sKV + slot_of(fk) * L::kKVBytes);
+          issue_qk(tS1, sQ + L::kQBytes, sKV + slot_of(0) * L::kKVBytes);
           umma_commit(bar(L::S_FULL + 1));
-          umma_commit(bar(L::KV_EMPTY + slot_of(fk)));
+          umma_commit(bar(L::KV_EMPTY + slot_of(0)));
           issued = true;
-          if (j < nT0) {  // PV_0(j)
-            if (!wait_bar_warp(bar(L::KV_FULL + slot_of(fv)), par_of(fv), ctl) ||
-                !wait_bar_warp(bar(L::PV_READY + 0), j & 1, ctl)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            issue_pv(tO0, tS0, sKV + slot_of(fv) * L::kKVBytes, j > 0);
-            umma_commit(bar(L::O_READY + 0));
+        }
+      }
+#pragma unroll 1
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int fv = 2 * j + 1, fk_next = 2 * j + 2;
+        const bool has0 = j < nT0, next = j + 1 < n_kv, next0 = j + 1 < nT0;
+        if (next && !wait_bar_warp(bar(L::KV_FULL + slot_of(fk_next)), par_of(fk_next), ctl)) {
+          ok = false;
+          break;
+        }
+        if (!wait_bar_warp(bar(L::KV_FULL + slot_of(fv)), par_of(fv), ctl)) { ok = false; break; }
+        if (has0) {  // PV_0(j), then QK_0(j+1) over P_0(j)
+          if (!wait_bar_warp(bar(L::PV_READY + 0), j & 1, ctl)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv(tO0, tS0, sKV + slot_of(fv) * L::kKVBytes, j > 0);
+          umma_commit(bar(L::O_READY + 0));
+          if (next0) {
+            issue_qk(tS0, sQ, sKV + slot_of(fk_next) * L::kKVBytes);
+            umma_commit(bar(L::S_FULL + 0));
           }
+        }
+        // PV_1(j), then QK_1(j+1) over P_1(j)
+        if (!wait_bar_warp(bar(L::PV_READY + 1), j & 1, ctl)) { ok = false; break; }
+        tc_fence_after();
+        issue_pv(tO1, tS1, sKV + slot_of(fv) * L::kKVBytes, j > 0);
+        umma_commit(bar(L::O_READY + 1));
+        umma_commit(bar(L::KV_EMPTY + slot_of(fv)));
+        if (next) {
+          issue_qk(tS1, sQ + L::kQBytes, sKV + slot_of(fk_next) * L::kKVBytes);
+          umma_commit(bar(L::S_FULL + 1));
+          umma_commit(bar(L::KV_EMPTY + slot_of(fk_next)));
         }
       }
       if (issued) {  // every MMA issued so far completes before TMEM is freed
