@@ -294,26 +294,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 16; ++e)
             if (cc * 16 + e > lim) sr[cc][e] = __float_as_uint(-INFINITY);
       }
-      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+      // row max as a shallow tree: 16 independent 8-column maxima, then 3 levels
+      float mx[16];
 #pragma unroll
-      for (int cc = 0; cc < 8; ++cc)
-#pragma unroll
-        for (int e = 0; e < 16; e += 8) {
-          mx0 = fmax3(mx0, __uint_as_float(sr[cc][e + 0]), __uint_as_float(sr[cc][e + 1]));
-          mx1 = fmax3(mx1, __uint_as_float(sr[cc][e + 2]), __uint_as_float(sr[cc][e + 3]));
-          mx2 = fmax3(mx2, __uint_as_float(sr[cc][e + 4]), __uint_as_float(sr[cc][e + 5]));
-          mx3 = fmax3(mx3, __uint_as_float(sr[cc][e + 6]), __uint_as_float(sr[cc][e + 7]));
-        }
-      const float t_max = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+      for (int g = 0; g < 16; ++g) {
+        const uint32_t* v = &sr[g >> 1][(g & 1) * 8];
+        float a = fmax3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
+        a = fmax3(a, __uint_as_float(v[3]), __uint_as_float(v[4]));
+        a = fmax3(a, __uint_as_float(v[5]), __uint_as_float(v[6]));
+        mx[g] = fmaxf(a, __uint_as_float(v[7]));
+      }
+      const float r0 = fmax3(mx[0], mx[1], mx[2]), r1 = fmax3(mx[3], mx[4], mx[5]);
+      const float r2 = fmax3(mx[6], mx[7], mx[8]), r3 = fmax3(mx[9], mx[10], mx[11]);
+      const float r4 = fmax3(mx[12], mx[13], mx[14]);
+      const float t_max = fmaxf(fmax3(r0, r1, r2), fmax3(r3, r4, mx[15])) * c;
       // raise the reference max only past the threshold (m = -inf: always)
       const float m_new = t_max > m + tau ? t_max : m;
       const float m_use = m_new == -INFINITY ? 0.f : m_new;
       const float alpha = m_new == m ? 1.f : ex2_approx(m - m_use);
-      if (j > 0) {
-        alpha_smem[s * kBM + r] = alpha;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(L::A_READY + s));
-      }
       const float neg_m = -m_use;
       // p = 2^(s*c - m) in four 32-column pieces: the argument as packed
       // fp32x2 FMAs, the row sum as packed fp32x2 adds; each piece is packed
@@ -323,6 +321,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
+        if (h == 1 && j > 0) {
+          // alpha for the correction warpgroup, published once the first
+          // piece of P is on its way (it rarely has work: tau keeps the
+          // reference max still)
+          alpha_smem[s * kBM + r] = alpha;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(L::A_READY + s));
+        }
         uint32_t pk[16];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
