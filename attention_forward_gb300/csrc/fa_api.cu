@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -49,6 +50,13 @@ namespace {
 // Device status word: kernels record FA_ERR_TIMEOUT here.
 __device__ unsigned g_status_word;
 
+// Slots of the prefill kernel's item scheduler (see PrefillParams::sched);
+// zero at load, and cleared again by the last CTA of every launch.
+__device__ unsigned long long g_sched[2 * fa::kSchedSlots];
+// Prefill launches of this process, numbered to pick a scheduler slot: two
+// launches can share a slot only 1024 launches apart.
+std::atomic<unsigned> g_launch_seq{0};
+
 constexpr int kMaxDevices = 64;
 constexpr unsigned long long kDefaultWatchdogNs = 1000000000ull;
 std::atomic<unsigned long long> g_watchdog_ns{kDefaultWatchdogNs};
@@ -58,6 +66,7 @@ struct DeviceState {
   fa_status_t usable = FA_ERR_UNSUPPORTED;
   int sm_count = 0;
   unsigned* status = nullptr;
+  unsigned long long* sched = nullptr;  // g_sched on this device
   bool regs_ok[2][2] = {};  // [D==128][bf16]
   bool regs_checked[2][2] = {};
   void* workspace = nullptr;  // fa_fwd's cached decode workspace
@@ -101,11 +110,14 @@ fa_status_t current_device(DeviceState** out, int* dev_out) {
       d.usable = FA_ERR_UNSUPPORTED;
     } else {
       void* addr = nullptr;
-      if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) {
+      void* sched = nullptr;
+      if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess ||
+          cudaGetSymbolAddress(&sched, g_sched) != cudaSuccess) {
         d.probed = false;
         return FA_ERR_CUDA;
       }
       d.status = static_cast<unsigned*>(addr);
+      d.sched = static_cast<unsigned long long*>(sched);
       d.usable = FA_OK;
     }
   }
@@ -190,10 +202,13 @@ fa_status_t run_prefill(DeviceState& d, const void* q, const void* k, const void
   p.test_stall = (flags & FA_FLAG_TEST_STALL) ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.rescale_tau = (flags & FA_FLAG_EXACT_MAX) ? 0.f : 8.f;
-  const long long grid = static_cast<long long>(p.n_qtiles) * BH;
-  if (grid > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
-  if (fa::launch_prefill(D, bf16, tq, tk, tv, to, p, static_cast<int>(grid), stream) !=
-      cudaSuccess)
+  const long long n_items = static_cast<long long>(p.n_qtiles) * BH;
+  if (n_items > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  p.n_items = static_cast<int>(n_items);
+  p.sched = d.sched + 2 * (g_launch_seq.fetch_add(1) % fa::kSchedSlots);
+  // persistent: one CTA per SM (the kernel's shared memory allows no second)
+  const int grid = static_cast<int>(std::min<long long>(n_items, d.sm_count > 0 ? d.sm_count : 1));
+  if (fa::launch_prefill(D, bf16, tq, tk, tv, to, p, grid, stream) != cudaSuccess)
     return FA_ERR_CUDA;
   return FA_OK;
 }

@@ -10,23 +10,32 @@ namespace fa {
 constexpr unsigned kStatusOk = 0;
 constexpr unsigned kStatusTimeout = 5;
 
-// Prefill tiling: a CTA owns kStages query tiles of kBM rows (two ping-pong
-// stages) and walks the keys in tiles of kBN.
+// Prefill tiling: a work item is kStages query tiles of kBM rows (two
+// ping-pong stages) of one head, walked over the keys in tiles of kBN; a
+// persistent CTA per SM takes items in turn.
 constexpr int kBM = 128;
 constexpr int kBN = 128;
 constexpr int kStages = 2;
 constexpr int kRowsPerCta = kBM * kStages;
 constexpr int kThreads = 512;  // 4 warpgroups
 
+// Dynamic item scheduler: slots of a static device array, one per launch
+// (chosen round-robin by the host), two words each: [0] = items claimed,
+// [1] = CTAs finished.  Both are zero when a launch starts: the launch's
+// last CTA clears them.
+constexpr int kSchedSlots = 1024;
+
 struct PrefillParams {
   float* lse;                 // [B*H, Sq]
+  unsigned long long* sched;  // this launch's scheduler slot
   unsigned* status;           // device status word
   unsigned long long timeout_ns;
   int BH;                     // B*H
   int Sq, Skv;
   int n_qtiles;               // ceil(Sq / kRowsPerCta)
+  int n_items;                // n_qtiles * BH work items (256 rows of one head)
   int causal;
-  int lpt;                    // heaviest-first CTA order (causal only)
+  int lpt;                    // heaviest-first item order (causal only)
   int always_rescale;
   int test_stall;
   float scale_log2;           // scale * log2(e)

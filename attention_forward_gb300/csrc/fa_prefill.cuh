@@ -1,14 +1,19 @@
 // fa_prefill.cuh -- fused attention forward (prefill) kernel for sm_103a.
 //
-// One CTA owns 256 query rows of one (batch, head) as two ping-pong stages of
-// 128 rows (the two-Q-tile ping-pong of the B300 G5 page, V21) and streams
-// the keys in tiles of 128.  Warp roles (16 warps, 512 threads):
+// A persistent CTA per SM works through items: an item is 256 query rows of
+// one (batch, head), as two ping-pong stages of 128 rows (the two-Q-tile
+// ping-pong of the B300 G5 page, V21), streamed over the keys in tiles of
+// 128.  Items are claimed at run time, heaviest first under causal masking
+// (LPT, "The FA5090 Optimization Journey" section 2.7).  Warp roles (16
+// warps, 512 threads):
 //
-//   warps 0-3   softmax, stage 0   one thread per query row (TMEM lane)
+//   warps 0-3   softmax, stage 0   one thread per query row (TMEM lane); also
+//                                  rescales O when a row's reference max moves
 //   warps 4-7   softmax, stage 1
-//   warps 8-11  correction: rescales O in TMEM when a row's reference max moved
+//   warps 8-11  epilogue: O / l to 16 bits, staged in smem, stored by TMA
 //   warp  12    tcgen05.mma issue (whole warp, one elected lane) + TMEM alloc
-//   warp  13    TMA producer (one thread): Q once, then K/V tiles
+//   warp  13    TMA producer (one thread) and item scheduler: claims items,
+//               loads each item's Q and then its K/V tiles into a ring
 //   warps 14-15 idle (they complete the fourth warpgroup)
 //
 // Tensor memory (512 columns x 128 lanes): S_s = Q_s K^T at columns s*128
@@ -21,19 +26,22 @@
 // Issue order of the tensor core: QK_0(0) QK_1(0), then per key tile j
 //     PV_0(j)  QK_0(j+1)  PV_1(j)  QK_1(j+1)
 // so that each softmax warpgroup has two GEMMs of the other stage to hide
-// behind (the aim of the ping-pong on the G5 page).  K and V occupy separate
-// slots of one ring with their own full/empty barriers (the decoupled K/V
-// loads of G5 V26), and stage 0's PV never waits for stage 1 (the PV0
-// barrier of V30).
+// behind (the aim of the ping-pong on the G5 page); at an item's last tile
+// the next item's QK_s(0) take the place of QK_s(j+1), so the tensor core
+// goes on while the epilogue warps store the finished item.  K and V occupy
+// separate slots of one ring with their own full/empty barriers (the
+// decoupled K/V loads of G5 V26), and stage 0's PV never waits for stage 1
+// (the PV0 barrier of V30).
 //
 // Softmax works in the log2 domain with the scale folded into one FFMA
-// before ex2 (G5 V33 "log2exp2"; "The FA5090 Optimization Journey" section
-// 2.6): t = s*scale*log2(e), p = 2^(t - m) against a per-row reference max m.
-// m is raised only when the tile's max exceeds it by more than tau (log2
-// units); then alpha = 2^(m_old - m_new) and the correction warpgroup
-// multiplies O by alpha, skipping any warp whose 32 rows all have alpha == 1
-// (a warp-uniform vote).  tau = 0 is the identity-only rescale skip of the
-// FA5090 page (sections 2.6 and 2.8: skip exactly when the max did not
+// before ex2 (G5 V33 "log2exp2"; FA5090 section 2.6): t = s*scale*log2(e),
+// p = 2^(t - m) against a per-row reference max m.  m is raised only when
+// the tile's max exceeds it by more than tau (log2 units); then
+// alpha = 2^(m_old - m_new) and the softmax warp multiplies its rows of O by
+// alpha before releasing the next PV, skipping it when all 32 rows of the
+// warp have alpha == 1 (a warp-uniform vote; the correction merged into the
+// softmax warpgroup, G5 V25).  tau = 0 is the identity-only rescale skip of
+// the FA5090 page (sections 2.6 and 2.8: skip exactly when the max did not
 // change); tau = 8 is FA4's lazy rescale that the same page describes in
 // section 3 (p stays <= 2^8, and the final division by l, accumulated
 // against the same m, makes the result exact either way).
@@ -41,8 +49,7 @@
 // Causal (bottom-right): key tiles past the last row's diagonal are never
 // loaded or computed (FA5090 section 2.7, causal block skip); only tiles that
 // cross the diagonal (or the ragged end of the keys) are masked (section
-// 2.8, diagonal-only masking).  CTAs are ordered heaviest-first (LPT,
-// section 2.7).
+// 2.8, diagonal-only masking).
 //
 // Every mbarrier wait is bounded by a watchdog; a wait that runs out sets a
 // shared abort flag and the device status word, every role leaves its loop,
@@ -57,35 +64,54 @@
 
 namespace fa {
 
+// Items in flight between the producer, which claims them, and the other
+// roles, which take them in the same order.
+constexpr int kItemRing = 4;
+// Warps that take every item: the MMA warp, 8 softmax warps, 4 epilogue warps.
+constexpr int kItemTakers = 13;
+
 template <int D>
 struct PrefillLayout {
   static_assert(D == 64 || D == 128, "head dim");
   static constexpr int kQBytes = kBM * D * 2;    // one stage of Q
   static constexpr int kKVBytes = kBN * D * 2;   // one K or V tile
   static constexpr int kBox = 128 * 64 * 2;      // one TMA box (64 cols)
-  static constexpr int kSlots = D == 128 ? 5 : 11;
+  static constexpr int kSlots = D == 128 ? 4 : 11;
+  static constexpr int kOutWarpBytes = 32 * D * 2;  // one epilogue warp's 32 rows of O
+  static constexpr int kOutBox = 32 * 64 * 2;       // one 64-column box of them
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = kOffQ + kStages * kQBytes;
-  static constexpr int kOffMisc = kOffKV + kSlots * kKVBytes;
+  static constexpr int kOffOut = kOffKV + kSlots * kKVBytes;
+  static constexpr int kOffMisc = kOffOut + 4 * kOutWarpBytes;
   // mbarrier indices
-  static constexpr int Q_FULL = 0;    // [2]
-  static constexpr int S_FULL = 2;    // [2]
-  static constexpr int PV_READY = 4;  // [2] P stored and O rescaled
-  static constexpr int A_READY = 6;   // [2]
-  static constexpr int O_READY = 8;   // [2]
-  static constexpr int DRAIN = 10;
-  static constexpr int KV_FULL = 11;            // [kSlots]
-  static constexpr int KV_EMPTY = 11 + kSlots;  // [kSlots]
-  static constexpr int kNumBars = 11 + 2 * kSlots;
+  static constexpr int Q_FULL = 0;    // [2] Q_s of the current item landed
+  static constexpr int Q_EMPTY = 2;   // [2] the item's last QK_s is done: Q_s reusable
+  static constexpr int S_FULL = 4;    // [2] S_s = Q_s K^T ready
+  static constexpr int PV_READY = 6;  // [2] P_s stored (and O_s rescaled)
+  static constexpr int O_READY = 8;   // [2] PV_s done
+  static constexpr int ML_FULL = 10;  // [2] the item's 1/l published
+  static constexpr int O_FREE = 12;   // [2] the epilogue has read O_s
+  static constexpr int DRAIN = 14;
+  static constexpr int ITEM_FULL = 15;   // [kItemRing] next item index published
+  static constexpr int ITEM_EMPTY = 19;  // [kItemRing] every role has read it
+  static constexpr int KV_FULL = 23;            // [kSlots]
+  static constexpr int KV_EMPTY = 23 + kSlots;  // [kSlots]
+  static constexpr int kNumBars = 23 + 2 * kSlots;
   static constexpr int kOffBars = kOffMisc;
-  static constexpr int kOffAlpha = kOffBars + ((kNumBars * 8 + 15) / 16) * 16;
-  static constexpr int kOffTmemSlot = kOffAlpha + kStages * kBM * 4;
+  static constexpr int kOffInvL = kOffBars + ((kNumBars * 8 + 15) / 16) * 16;
+  static constexpr int kOffItems = kOffInvL + kStages * kBM * 4;
+  static constexpr int kOffTmemSlot = kOffItems + kItemRing * 4;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kMiscBytes = kOffAbort + 4 - kOffMisc;
   static constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;  // + align
   static constexpr int kTmemCols = 512;
   static constexpr int kTmemO = 256;  // O_s at column 256 + s*D
   static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+// One work item: 256 query rows (two stages) of one (batch, head).
+struct Item {
+  int bh, row0, nT0, nT1;
 };
 
 // Register split between warpgroups (setmaxnreg): softmax warpgroups get
@@ -103,20 +129,36 @@ struct Ctl {
   unsigned long long timeout;
 };
 
-// try_wait suspends the thread for a while before it reports "not yet", so
-// the abort flag and the clock are checked only every 8th round.
-__device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, Ctl c) {
+// Back-off between polls, per role.  A warp polling an mbarrier takes issue
+// slots from the softmax warps that share its SM sub-partition (each
+// sub-partition runs one softmax warp of each stage), and the softmax is on
+// the critical path; so every role but the softmax sleeps between polls.
+// The MMA warp's sleep is short (it reacts to the softmax's arrivals); the
+// producer runs a ring ahead and the epilogue warps wait a whole item.
+constexpr unsigned kSleepMmaNs = 32;
+constexpr unsigned kSleepProducerNs = 64;
+constexpr unsigned kSleepEpilogueNs = 256;
+
+// The slow path of a wait, out of line so that the loops that wait stay
+// small: try_wait suspends the thread for a short while before it reports
+// "not yet"; the abort flag and the clock are checked every 8th round.
+template <unsigned kSleepNs>
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity,
+                                       volatile uint32_t* abort_flag,
+                                       unsigned* status,
+                                       unsigned long long timeout) {
   uint64_t t0 = 0;
   for (uint32_t n = 1;; ++n) {
+    if constexpr (kSleepNs > 0) __nanosleep(kSleepNs);
     if (mbar_try_wait(bar, parity)) return true;
     if ((n & 7u) == 0) {
-      if (*c.abort) return false;
+      if (*abort_flag) return false;
       const uint64_t t = globaltimer_ns();
       if (t0 == 0) {
         t0 = t;
-      } else if (t - t0 > c.timeout) {
-        *c.abort = 1u;
-        atomicExch(c.status, kStatusTimeout);
+      } else if (t - t0 > timeout) {
+        *abort_flag = 1u;
+        atomicExch(status, kStatusTimeout);
         return false;
       }
     }
@@ -124,15 +166,18 @@ __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, Ctl c) 
 }
 
 // Bounded wait; false when the watchdog fired (here or in another role).
+template <unsigned kSleepNs = 0>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity,
                                          const Ctl& c) {
-  return mbar_try_wait(bar, parity) || wait_slow(bar, parity, c);
+  return mbar_try_wait(bar, parity) ||
+         wait_slow<kSleepNs>(bar, parity, c.abort, c.status, c.timeout);
 }
 
 // Warp-uniform bounded wait (every lane gets the same answer).
+template <unsigned kSleepNs = 0>
 __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity,
                                               const Ctl& c) {
-  const bool ok = wait_bar(bar, parity, c);
+  const bool ok = wait_bar<kSleepNs>(bar, parity, c);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -174,6 +219,47 @@ __device__ __forceinline__ int stage_tiles(int row_first, int Sq, int Skv,
   return min(n_all, last_key / kBN + 1);
 }
 
+// Item idx (0 <= idx < n_items): heaviest first under causal LPT.
+__device__ __forceinline__ Item get_item(const PrefillParams& p, int idx) {
+  Item it;
+  int qtile;
+  if (p.causal && p.lpt) {
+    qtile = p.n_qtiles - 1 - idx / p.BH;
+    it.bh = idx % p.BH;
+  } else {
+    qtile = idx % p.n_qtiles;
+    it.bh = idx / p.n_qtiles;
+  }
+  it.row0 = qtile * kRowsPerCta;
+  it.nT0 = stage_tiles(it.row0, p.Sq, p.Skv, p.causal);
+  it.nT1 = stage_tiles(it.row0 + kBM, p.Sq, p.Skv, p.causal);
+  return it;
+}
+
+// Claims the next item for this CTA: a CTA starts with item blockIdx.x and
+// then takes items gridDim.x, gridDim.x + 1, ... in the order SMs free up
+// (with the heaviest-first numbering, the greedy LPT schedule).  One
+// fetch-and-add on the launch's scheduler slot, which starts at zero.
+// Returns -1 once every item is claimed.
+__device__ __forceinline__ int claim_item(const PrefillParams& p) {
+  const unsigned long long ticket = atomicAdd(p.sched, 1ull);
+  const unsigned long long idx = gridDim.x + ticket;
+  return idx < static_cast<unsigned long long>(p.n_items) ? static_cast<int>(idx) : -1;
+}
+
+// The k-th item of this CTA (-1: no more), as published by the producer.
+template <unsigned kSleepNs>
+__device__ __forceinline__ int take_item(const volatile int* ring, uint32_t full,
+                                         uint32_t empty, uint32_t k, const Ctl& c,
+                                         bool& ok) {
+  const uint32_t slot = k % kItemRing;
+  ok = wait_bar_warp<kSleepNs>(full + 8u * slot, (k / kItemRing) & 1, c);
+  const int idx = ok ? ring[slot] : -1;
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(empty + 8u * slot);
+  return idx;
+}
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_prefill_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -188,8 +274,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sQ = sbase + L::kOffQ;
   const uint32_t sKV = sbase + L::kOffKV;
+  const uint32_t sOut = sbase + L::kOffOut;
   const uint32_t bars = sbase + L::kOffBars;
-  float* alpha_smem = reinterpret_cast<float*>(smem + L::kOffAlpha);
+  float* inv_l_smem = reinterpret_cast<float*>(smem + L::kOffInvL);
+  volatile int* item_ring = reinterpret_cast<volatile int*>(smem + L::kOffItems);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffTmemSlot);
   volatile uint32_t* abort_flag =
       reinterpret_cast<volatile uint32_t*>(smem + L::kOffAbort);
@@ -198,30 +286,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- work item (heaviest-first for causal) ----
-  int qtile, bh;
-  if (p.causal && p.lpt) {
-    qtile = p.n_qtiles - 1 - static_cast<int>(blockIdx.x) / p.BH;
-    bh = static_cast<int>(blockIdx.x) % p.BH;
-  } else {
-    qtile = static_cast<int>(blockIdx.x) % p.n_qtiles;
-    bh = static_cast<int>(blockIdx.x) / p.n_qtiles;
-  }
-  const int row0 = qtile * kRowsPerCta;
-  const int nT0 = stage_tiles(row0, p.Sq, p.Skv, p.causal);
-  const int nT1 = stage_tiles(row0 + kBM, p.Sq, p.Skv, p.causal);
-  const int n_kv = nT1;  // nT1 >= nT0
-
-  // ---- setup ----
+  // ---- setup (once per CTA; every barrier's phase runs on across items) ----
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(L::Q_FULL + s), 1);
+      mbar_init(bar(L::Q_EMPTY + s), 1);
       mbar_init(bar(L::S_FULL + s), 1);
-      mbar_init(bar(L::PV_READY + s), 8);  // 4 softmax warps + 4 correction warps
-      mbar_init(bar(L::A_READY + s), 4);
+      mbar_init(bar(L::PV_READY + s), 4);  // the stage's 4 softmax warps
       mbar_init(bar(L::O_READY + s), 1);
+      mbar_init(bar(L::ML_FULL + s), 4);
+      mbar_init(bar(L::O_FREE + s), 4);    // the 4 epilogue warps
     }
     mbar_init(bar(L::DRAIN), 1);
+    for (int i = 0; i < kItemRing; ++i) {
+      mbar_init(bar(L::ITEM_FULL + i), 1);
+      mbar_init(bar(L::ITEM_EMPTY + i), kItemTakers);
+    }
     for (int i = 0; i < L::kSlots; ++i) {
       mbar_init(bar(L::KV_FULL + i), 1);
       mbar_init(bar(L::KV_EMPTY + i), 1);
@@ -257,115 +337,172 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int s = wg;
     const int rq = warp & 3;                 // lane quarter of TMEM
     const int r = rq * 32 + lane;            // row within the stage
-    const int stage_row0 = row0 + s * kBM;
-    const int row_g = stage_row0 + r;        // query row
-    const int nT = s == 0 ? nT0 : nT1;
     const int off = p.Skv - p.Sq;
     const uint32_t t_lane = static_cast<uint32_t>(rq * 32) << 16;
     const uint32_t tS = tmem + t_lane + static_cast<uint32_t>(s * kBN);
     const uint32_t tO = tmem + t_lane + static_cast<uint32_t>(L::kTmemO + s * D);
     const float c = p.scale_log2;
     const float tau = p.rescale_tau;
-    float m = -INFINITY;  // reference max of c*s (log2 units)
-    float l = 0.f;        // running sum of 2^(c*s - m)
+    uint32_t n_s = 0;  // tiles of this stage so far (S_FULL / O_READY phase)
     bool ok = true;
 
 #pragma unroll 1
-    for (int j = 0; j < nT; ++j) {
-      if (!wait_bar_warp(bar(L::S_FULL + s), j & 1, ctl)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t sr[8][16];
-#pragma unroll
-      for (int cc = 0; cc < 8; ++cc) tmem_ld16(tS + cc * 16, sr[cc]);
-      tmem_wait_ld();
-#pragma unroll
-      for (int cc = 0; cc < 8; ++cc) reg_fence16(sr[cc]);
+    for (uint32_t k = 0; ok; ++k) {
+      const int idx = take_item<0>(item_ring, bar(L::ITEM_FULL), bar(L::ITEM_EMPTY), k, ctl, ok);
+      if (!ok || idx < 0) break;
+      const Item it = get_item(p, idx);
+      const int nT = s == 0 ? it.nT0 : it.nT1;
+      const int stage_row0 = it.row0 + s * kBM;
+      const int row_g = stage_row0 + r;        // query row
+      float m = -INFINITY;  // reference max of c*s (log2 units)
+      float l = 0.f;        // running sum of 2^(c*s - m)
 
-      // mask: ragged key tail, and the causal diagonal
-      const int key0 = j * kBN;
-      const bool need_mask =
-          (key0 + kBN > p.Skv) || (p.causal && key0 + kBN - 1 > stage_row0 + off);
-      if (need_mask) {
-        int lim = p.Skv - 1 - key0;
-        if (p.causal) lim = min(lim, row_g + off - key0);
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc)
-#pragma unroll
-          for (int e = 0; e < 16; ++e)
-            if (cc * 16 + e > lim) sr[cc][e] = __float_as_uint(-INFINITY);
-      }
-      // row max as a shallow tree: 16 independent 8-column maxima, then 3 levels
-      float mx[16];
-#pragma unroll
-      for (int g = 0; g < 16; ++g) {
-        const uint32_t* v = &sr[g >> 1][(g & 1) * 8];
-        float a = fmax3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
-        a = fmax3(a, __uint_as_float(v[3]), __uint_as_float(v[4]));
-        a = fmax3(a, __uint_as_float(v[5]), __uint_as_float(v[6]));
-        mx[g] = fmaxf(a, __uint_as_float(v[7]));
-      }
-      const float r0 = fmax3(mx[0], mx[1], mx[2]), r1 = fmax3(mx[3], mx[4], mx[5]);
-      const float r2 = fmax3(mx[6], mx[7], mx[8]), r3 = fmax3(mx[9], mx[10], mx[11]);
-      const float r4 = fmax3(mx[12], mx[13], mx[14]);
-      const float t_max = fmaxf(fmax3(r0, r1, r2), fmax3(r3, r4, mx[15])) * c;
-      // raise the reference max only past the threshold (m = -inf: always)
-      const float m_new = t_max > m + tau ? t_max : m;
-      const float m_use = m_new == -INFINITY ? 0.f : m_new;
-      const float alpha = m_new == m ? 1.f : ex2_approx(m - m_use);
-      const float neg_m = -m_use;
-      // p = 2^(s*c - m) in four 32-column pieces: the argument as packed
-      // fp32x2 FMAs, the row sum as packed fp32x2 adds; each piece is packed
-      // to 16-bit pairs and stored over the first 64 columns of S_s (every S
-      // value of this row is already in registers) while the next piece's
-      // exponentials run
-      float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        if (h == 1 && j > 0) {
-          // alpha for the correction warpgroup, published once the first
-          // piece of P is on its way (it rarely has work: tau keeps the
-          // reference max still)
-          alpha_smem[s * kBM + r] = alpha;
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(L::A_READY + s));
-        }
-        uint32_t pk[16];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int col = h * 32 + q * 4;
-          uint32_t* v = &sr[col >> 4][col & 15];
-          float x0, x1, x2, x3;
-          ffma2(x0, x1, __uint_as_float(v[0]), __uint_as_float(v[1]), c, c, neg_m, neg_m);
-          ffma2(x2, x3, __uint_as_float(v[2]), __uint_as_float(v[3]), c, c, neg_m, neg_m);
-          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-          const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
-          fadd2(l0, l1, l0, l1, p0, p1);
-          fadd2(l2, l3, l2, l3, p2, p3);
-          pk[2 * q] = pack2<BF16>(p0, p1);
-          pk[2 * q + 1] = pack2<BF16>(p2, p3);
-        }
-        tmem_st16(tS + h * 16, pk);
-      }
-      l = l * alpha + ((l0 + l1) + (l2 + l3));
-      m = m_new;
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::PV_READY + s));
-    }
-
-    // ------------------------------ epilogue ------------------------------
-    if (ok) {
-      const bool have_o = nT > 0;
-      // the Q_s buffer becomes the output staging buffer: its TMA load must
-      // have landed (a stage with no key tile never waited for it), and the
-      // last PV_s must have completed (it also ends every QK_s read of Q_s)
-      ok = wait_bar_warp(bar(L::Q_FULL + s), 0, ctl);
-      if (ok && have_o) ok = wait_bar_warp(bar(L::O_READY + s), (nT - 1) & 1, ctl);
-      if (ok) {
+#pragma unroll 1
+      for (int j = 0; j < nT; ++j, ++n_s) {
+        if (!wait_bar_warp(bar(L::S_FULL + s), n_s & 1, ctl)) { ok = false; break; }
         tc_fence_after();
-        const float inv_l = l > 0.f ? 1.f / l : 0.f;
-        const uint32_t stage_buf = sQ + static_cast<uint32_t>(s * L::kQBytes);
+        uint32_t sr[8][16];
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) tmem_ld16(tS + cc * 16, sr[cc]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) reg_fence16(sr[cc]);
+
+        // mask: ragged key tail, and the causal diagonal
+        const int key0 = j * kBN;
+        const bool need_mask =
+            (key0 + kBN > p.Skv) || (p.causal && key0 + kBN - 1 > stage_row0 + off);
+        if (need_mask) {
+          int lim = p.Skv - 1 - key0;
+          if (p.causal) lim = min(lim, row_g + off - key0);
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc)
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              if (cc * 16 + e > lim) sr[cc][e] = __float_as_uint(-INFINITY);
+        }
+        // row max as a shallow tree: 16 independent 8-column maxima, then 3 levels
+        float mx[16];
+#pragma unroll
+        for (int g = 0; g < 16; ++g) {
+          const uint32_t* v = &sr[g >> 1][(g & 1) * 8];
+          float a = fmax3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
+          a = fmax3(a, __uint_as_float(v[3]), __uint_as_float(v[4]));
+          a = fmax3(a, __uint_as_float(v[5]), __uint_as_float(v[6]));
+          mx[g] = fmaxf(a, __uint_as_float(v[7]));
+        }
+        const float r0 = fmax3(mx[0], mx[1], mx[2]), r1 = fmax3(mx[3], mx[4], mx[5]);
+        const float r2 = fmax3(mx[6], mx[7], mx[8]), r3 = fmax3(mx[9], mx[10], mx[11]);
+        const float r4 = fmax3(mx[12], mx[13], mx[14]);
+        const float t_max = fmaxf(fmax3(r0, r1, r2), fmax3(r3, r4, mx[15])) * c;
+        // raise the reference max only past the threshold (m = -inf: always)
+        const float m_new = t_max > m + tau ? t_max : m;
+        const float m_use = m_new == -INFINITY ? 0.f : m_new;
+        const float alpha = m_new == m ? 1.f : ex2_approx(m - m_use);
+        const float neg_m = -m_use;
+        // p = 2^(s*c - m) in four 32-column pieces: the argument as packed
+        // fp32x2 FMAs, the row sum as packed fp32x2 adds; each piece is packed
+        // to 16-bit pairs and stored over the first 64 columns of S_s (every S
+        // value of this row is already in registers) while the next piece's
+        // exponentials run
+        float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const int col = h * 32 + q * 4;
+            uint32_t* v = &sr[col >> 4][col & 15];
+            float x0, x1, x2, x3;
+            ffma2(x0, x1, __uint_as_float(v[0]), __uint_as_float(v[1]), c, c, neg_m, neg_m);
+            ffma2(x2, x3, __uint_as_float(v[2]), __uint_as_float(v[3]), c, c, neg_m, neg_m);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+            fadd2(l0, l1, l0, l1, p0, p1);
+            fadd2(l2, l3, l2, l3, p2, p3);
+            pk[2 * q] = pack2<BF16>(p0, p1);
+            pk[2 * q + 1] = pack2<BF16>(p2, p3);
+          }
+          tmem_st16(tS + h * 16, pk);
+        }
+        l = l * alpha + ((l0 + l1) + (l2 + l3));
+        m = m_new;
+        // O_s *= alpha when a row of this warp moved its reference max (rare:
+        // tau keeps it still).  PV_s(j-1) has completed: S_FULL_s(j) was
+        // committed after it.  Tile 0 has no O of this item to rescale.
+        if (j > 0 && (p.always_rescale || __any_sync(0xffffffffu, alpha != 1.f))) {
+#pragma unroll 1
+          for (int cc = 0; cc < D / 16; ++cc) {
+            uint32_t v[16];
+            tmem_ld16(tO + cc * 16, v);
+            tmem_wait_ld();
+            reg_fence16(v);
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+            tmem_st16(tO + cc * 16, v);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(L::PV_READY + s));
+      }
+      if (!ok) break;
+
+      // end of the item: LSE straight to global, 1/l to the epilogue warps
+      // once the item's last PV_s has completed (then O_s is final)
+      if (row_g < p.Sq) {
+        const float lse = l > 0.f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+        p.lse[static_cast<size_t>(it.bh) * p.Sq + row_g] = lse;
+      }
+      if (nT > 0) {
+        if (!wait_bar_warp(bar(L::O_READY + s), (n_s - 1) & 1, ctl)) { ok = false; break; }
+        inv_l_smem[s * kBM + r] = l > 0.f ? 1.f / l : 0.f;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(L::ML_FULL + s));
+      }
+    }
+    __syncwarp();
+  } else if (wg == 2) {
+    // =============================== epilogue ===============================
+    // Per item and stage: O_s * (1/l), rounded to 16 bits, staged in this
+    // warp's 32-row slice of shared memory and written by TMA.  The warp
+    // arrives on O_FREE_s as soon as it has read O_s out of tensor memory,
+    // which lets the next item's first PV_s overwrite it.
+    const int rq = warp & 3;
+    const int r = rq * 32 + lane;
+    const uint32_t t_lane = static_cast<uint32_t>(rq * 32) << 16;
+    const uint32_t stage_buf = sOut + static_cast<uint32_t>(rq * L::kOutWarpBytes);
+    uint32_t n_t0 = 0, n_t1 = 0;  // tiles of stage s so far (O_READY phase)
+    uint32_t n_e0 = 0, n_e1 = 0;  // ML_FULL phases
+    bool ok = true;
+#pragma unroll 1
+    for (uint32_t k = 0; ok; ++k) {
+      const int idx = take_item<kSleepEpilogueNs>(item_ring, bar(L::ITEM_FULL),
+                                                  bar(L::ITEM_EMPTY), k, ctl, ok);
+      if (!ok || idx < 0) break;
+      const Item it = get_item(p, idx);
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        if (!ok) continue;
+        const int nT = s == 0 ? it.nT0 : it.nT1;
+        const bool have_o = nT > 0;
+        float inv_l = 0.f;
+        if (have_o) {
+          uint32_t& n_t = s == 0 ? n_t0 : n_t1;
+          uint32_t& n_e = s == 0 ? n_e0 : n_e1;
+          n_t += static_cast<uint32_t>(nT);
+          if (!wait_bar_warp<kSleepEpilogueNs>(bar(L::ML_FULL + s), n_e & 1, ctl)) { ok = false; continue; }
+          ++n_e;
+          inv_l = inv_l_smem[s * kBM + r];
+          if (!wait_bar_warp<kSleepEpilogueNs>(bar(L::O_READY + s), (n_t - 1) & 1, ctl)) { ok = false; continue; }
+          tc_fence_after();
+        }
+        // the slice is free once the previous store has read it
+        if (lane == 0) bulk_wait_group_read0();
+        __syncwarp();
+        const uint32_t tO = tmem + t_lane + static_cast<uint32_t>(L::kTmemO + s * D);
 #pragma unroll 1
         for (int cc = 0; cc < D / 16; ++cc) {
           uint32_t v[16];
@@ -373,89 +510,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld16(tO + cc * 16, v);
             tmem_wait_ld();
             reg_fence16(v);
-          } else {
+          } else {  // no visible key: O = 0
 #pragma unroll
             for (int e = 0; e < 16; ++e) v[e] = 0u;
           }
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const int col = cc * 16 + h * 8;  // first column of this chunk
+            const int col = cc * 16 + h * 8;  // first column of this 16-byte chunk
             const uint32_t w0 = pack2<BF16>(__uint_as_float(v[h * 8 + 0]) * inv_l, __uint_as_float(v[h * 8 + 1]) * inv_l);
             const uint32_t w1 = pack2<BF16>(__uint_as_float(v[h * 8 + 2]) * inv_l, __uint_as_float(v[h * 8 + 3]) * inv_l);
             const uint32_t w2 = pack2<BF16>(__uint_as_float(v[h * 8 + 4]) * inv_l, __uint_as_float(v[h * 8 + 5]) * inv_l);
             const uint32_t w3 = pack2<BF16>(__uint_as_float(v[h * 8 + 6]) * inv_l, __uint_as_float(v[h * 8 + 7]) * inv_l);
             const int box = col >> 6, chunk = (col & 63) >> 3;
-            const uint32_t addr = stage_buf + static_cast<uint32_t>(
-                                                  box * L::kBox + r * 128 + ((chunk ^ (r & 7)) << 4));
-            st_shared_v4(addr, w0, w1, w2, w3);
+            st_shared_v4(stage_buf + static_cast<uint32_t>(box * L::kOutBox + lane * 128 +
+                                                           ((chunk ^ (lane & 7)) << 4)),
+                         w0, w1, w2, w3);
           }
+        }
+        if (have_o) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(L::O_FREE + s));
         }
         fence_proxy_async_smem();
         __syncwarp();
-        const int warp_row0 = stage_row0 + rq * 32;
+        const int warp_row0 = it.row0 + s * kBM + rq * 32;
         if (lane == 0 && warp_row0 < p.Sq) {
 #pragma unroll
           for (int box = 0; box < D / 64; ++box)
-            tma_store_3d(&tmO, stage_buf + static_cast<uint32_t>(box * L::kBox + rq * 32 * 128),
-                         box * 64, warp_row0, bh);
+            tma_store_3d(&tmO, stage_buf + static_cast<uint32_t>(box * L::kOutBox), box * 64,
+                         warp_row0, it.bh);
           bulk_commit_group();
-          bulk_wait_group0();
-        }
-        if (row_g < p.Sq) {
-          const float lse = l > 0.f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
-          p.lse[static_cast<size_t>(bh) * p.Sq + row_g] = lse;
         }
       }
     }
-    __syncwarp();
-  } else if (wg == 2) {
-    // ============================== correction ==============================
-    // For every key tile j of stage s: once softmax has published alpha and
-    // PV_s(j-1) has completed, rescale O_s if any row of this warp moved its
-    // reference max, then arrive on PV_READY_s (together with the softmax
-    // warps' arrival after storing P, that releases PV_s(j)).  Tile 0 has no
-    // O to rescale and only arrives.
-    const int rq = warp & 3;
-    const int r = rq * 32 + lane;
-    const uint32_t t_lane = static_cast<uint32_t>(rq * 32) << 16;
-#pragma unroll 1
-    for (int j = 0; j < n_kv; ++j) {
-      bool ok = true;
-#pragma unroll 1
-      for (int s = 0; s < 2; ++s) {
-        if (j >= (s == 0 ? nT0 : nT1)) continue;
-        if (j > 0) {
-          if (!wait_bar_warp(bar(L::A_READY + s), (j - 1) & 1, ctl)) { ok = false; break; }
-          const float alpha = alpha_smem[s * kBM + r];
-          if (!wait_bar_warp(bar(L::O_READY + s), (j - 1) & 1, ctl)) { ok = false; break; }
-          tc_fence_after();
-          if (p.always_rescale || __any_sync(0xffffffffu, alpha != 1.f)) {
-            const uint32_t tO = tmem + t_lane + static_cast<uint32_t>(L::kTmemO + s * D);
-#pragma unroll 1
-            for (int cc = 0; cc < D / 16; cc += 2) {
-              uint32_t v0[16], v1[16];
-              tmem_ld16(tO + cc * 16, v0);
-              tmem_ld16(tO + cc * 16 + 16, v1);
-              tmem_wait_ld();
-              reg_fence16(v0);
-              reg_fence16(v1);
-#pragma unroll
-              for (int e = 0; e < 16; ++e) {
-                v0[e] = __float_as_uint(__uint_as_float(v0[e]) * alpha);
-                v1[e] = __float_as_uint(__uint_as_float(v1[e]) * alpha);
-              }
-              tmem_st16(tO + cc * 16, v0);
-              tmem_st16(tO + cc * 16 + 16, v1);
-            }
-            tmem_wait_st();
-          }
-          tc_fence_before();
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(L::PV_READY + s));
-      }
-      if (!ok) break;
-    }
+    if (lane == 0) bulk_wait_group0();  // every store has landed before exit
     __syncwarp();
   } else if (warp == 12) {
     // ============================== MMA issuer ==============================
@@ -467,75 +556,148 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tS0 = tmem, tS1 = tmem + kBN;
       const uint32_t tO0 = tmem + L::kTmemO, tO1 = tmem + L::kTmemO + D;
       bool issued = false;
-      bool ok = wait_bar_warp(bar(L::Q_FULL + 0), 0, ctl) &&
-                wait_bar_warp(bar(L::Q_FULL + 1), 0, ctl);
 
-      // one asm block per GEMM: K = D for QK (both operands K-major in
-      // smem), K = 128 keys for PV (A = P_s from tensor memory, B = V MN-major)
-      auto issue_qk = [&](uint32_t d_tmem, uint32_t qbuf, uint32_t kbuf) {
-        const uint64_t da = smem_desc_sw128(qbuf, 16, 1024);
-        const uint64_t db = smem_desc_sw128(kbuf, 16, 1024);
-        if constexpr (D == 128) {
-          umma_f16_ss_k128(d_tmem, da, db, kIdescQK, 0u);
-        } else {
-          umma_f16_ss_k64(d_tmem, da, db, kIdescQK, 0u);
-        }
-      };
-      auto issue_pv = [&](uint32_t d_tmem, uint32_t p_tmem, uint32_t vbuf, bool acc) {
-        umma_f16_ts_k128(d_tmem, p_tmem, smem_desc_sw128(vbuf, L::kBox, 1024), kIdescPV,
-                         acc ? 1u : 0u);
-      };
       auto slot_of = [&](int fill) { return fill % L::kSlots; };
       auto par_of = [&](int fill) { return static_cast<uint32_t>((fill / L::kSlots) & 1); };
-
-      // Tensor-core order: QK_0(0) QK_1(0), then per key tile j
-      //   PV_0(j) QK_0(j+1) PV_1(j) QK_1(j+1)
-      // Each QK_s(j+1) follows PV_s(j) at once (it overwrites P_s(j)); the
-      // wait for K_(j+1) is done earlier, while the softmax of tile j runs.
-      if (n_kv > 0) {
-        ok = wait_bar_warp(bar(L::KV_FULL + slot_of(0)), par_of(0), ctl);
-        if (ok) {
-          tc_fence_after();
-          if (nT0 > 0) {
-            issue_qk(tS0, sQ, sKV + slot_of(0) * L::kKVBytes);
-            umma_commit(bar(L::S_FULL + 0));
-          }
-          issue_qk(tS1, sQ + L::kQBytes, sKV + slot_of(0) * L::kKVBytes);
-          umma_commit(bar(L::S_FULL + 1));
-          umma_commit(bar(L::KV_EMPTY + slot_of(0)));
-          issued = true;
+      // QK_s with K from fill fk: one asm block, K = D, both operands K-major
+      // in smem; commits S_FULL_s, and Q_EMPTY_s after the item's last QK_s
+      auto qk = [&](int s, int fk, bool last_of_stage) {
+        const uint64_t da = smem_desc_sw128(sQ + static_cast<uint32_t>(s * L::kQBytes), 16, 1024);
+        const uint64_t db = smem_desc_sw128(sKV + static_cast<uint32_t>(slot_of(fk) * L::kKVBytes), 16, 1024);
+        if constexpr (D == 128) {
+          umma_f16_ss_k128(s == 0 ? tS0 : tS1, da, db, kIdescQK, 0u);
+        } else {
+          umma_f16_ss_k64(s == 0 ? tS0 : tS1, da, db, kIdescQK, 0u);
         }
-      }
-#pragma unroll 1
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int fv = 2 * j + 1, fk_next = 2 * j + 2;
-        const bool has0 = j < nT0, next = j + 1 < n_kv, next0 = j + 1 < nT0;
-        if (next && !wait_bar_warp(bar(L::KV_FULL + slot_of(fk_next)), par_of(fk_next), ctl)) {
-          ok = false;
-          break;
-        }
-        if (!wait_bar_warp(bar(L::KV_FULL + slot_of(fv)), par_of(fv), ctl)) { ok = false; break; }
-        if (has0) {  // PV_0(j), then QK_0(j+1) over P_0(j)
-          if (!wait_bar_warp(bar(L::PV_READY + 0), j & 1, ctl)) { ok = false; break; }
-          tc_fence_after();
-          issue_pv(tO0, tS0, sKV + slot_of(fv) * L::kKVBytes, j > 0);
-          umma_commit(bar(L::O_READY + 0));
-          if (next0) {
-            issue_qk(tS0, sQ, sKV + slot_of(fk_next) * L::kKVBytes);
-            umma_commit(bar(L::S_FULL + 0));
-          }
-        }
-        // PV_1(j), then QK_1(j+1) over P_1(j)
-        if (!wait_bar_warp(bar(L::PV_READY + 1), j & 1, ctl)) { ok = false; break; }
+        umma_commit(bar(L::S_FULL + s));
+        if (last_of_stage) umma_commit(bar(L::Q_EMPTY + s));
+      };
+      // PV_s: K = 128 keys, A = P_s from tensor memory, B = V MN-major
+      auto pv = [&](int s, int fv, bool acc) {
+        umma_f16_ts_k128(s == 0 ? tO0 : tO1, s == 0 ? tS0 : tS1,
+                         smem_desc_sw128(sKV + static_cast<uint32_t>(slot_of(fv) * L::kKVBytes),
+                                         L::kBox, 1024),
+                         kIdescPV, acc ? 1u : 0u);
+        umma_commit(bar(L::O_READY + s));
+      };
+      // First QKs of an item whose Q is in buffer phase kq and whose K_0 is
+      // fill f (used for the CTA's first item and after an item without keys)
+      auto begin = [&](const Item& it, int kq, int f) -> bool {
+        if (!wait_bar_warp<kSleepMmaNs>(bar(L::Q_FULL + 0), kq & 1, ctl) ||
+            !wait_bar_warp<kSleepMmaNs>(bar(L::Q_FULL + 1), kq & 1, ctl))
+          return false;
+        if (it.nT1 > 0 && !wait_bar_warp<kSleepMmaNs>(bar(L::KV_FULL + slot_of(f)), par_of(f), ctl)) return false;
         tc_fence_after();
-        issue_pv(tO1, tS1, sKV + slot_of(fv) * L::kKVBytes, j > 0);
-        umma_commit(bar(L::O_READY + 1));
-        umma_commit(bar(L::KV_EMPTY + slot_of(fv)));
-        if (next) {
-          issue_qk(tS1, sQ + L::kQBytes, sKV + slot_of(fk_next) * L::kKVBytes);
-          umma_commit(bar(L::S_FULL + 1));
-          umma_commit(bar(L::KV_EMPTY + slot_of(fk_next)));
+        if (it.nT0 > 0) qk(0, f, it.nT0 == 1); else umma_commit(bar(L::Q_EMPTY + 0));
+        if (it.nT1 > 0) {
+          qk(1, f, it.nT1 == 1);
+          umma_commit(bar(L::KV_EMPTY + slot_of(f)));
+        } else {
+          umma_commit(bar(L::Q_EMPTY + 1));
         }
+        issued = true;
+        return true;
+      };
+
+      // Tensor-core order within an item: QK_0(0) QK_1(0), then per key tile
+      //   PV_0(j) QK_0(j+1) PV_1(j) QK_1(j+1)
+      // and at an item's last tile the next item's QK_s(0) take the place of
+      // QK_s(j+1), so the tensor core moves on while this item's epilogue
+      // runs; the next item's PV_s(0) also waits for O_FREE_s.
+      uint32_t n_pv0 = 0, n_pv1 = 0;  // PV_s issued so far (PV_READY phase)
+      uint32_t n_o0 = 0, n_o1 = 0;    // items so far with a PV_s (O_FREE phase)
+      int kq = 0;                     // items begun (Q_FULL phase)
+      int fK = 0;                     // fill of the current item's K_0
+      bool ok = true;
+      const int first = take_item<kSleepMmaNs>(item_ring, bar(L::ITEM_FULL),
+                                               bar(L::ITEM_EMPTY), 0, ctl, ok);
+      Item cur = first >= 0 ? get_item(p, first) : Item{0, 0, 0, 0};
+      if (ok && first >= 0) ok = begin(cur, 0, 0);
+      else ok = false;
+#pragma unroll 1
+      while (ok) {
+        // the next item is taken at this item's last key tile, once the
+        // producer has claimed it (it does so after the last K/V fill)
+        bool taken = false, has_next = false;
+        Item nxt{0, 0, 0, 0};
+        auto take_next = [&]() {
+          if (taken) return;
+          taken = true;
+          const int nidx = take_item<kSleepMmaNs>(item_ring, bar(L::ITEM_FULL),
+                                                  bar(L::ITEM_EMPTY), kq + 1, ctl, ok);
+          has_next = ok && nidx >= 0;
+          if (has_next) nxt = get_item(p, nidx);
+        };
+        const int fN = fK + 2 * cur.nT1;  // the next item's K_0
+#pragma unroll 1
+        for (int j = 0; j < cur.nT1; ++j) {
+          const bool last = j + 1 == cur.nT1;
+          if (last) {
+            take_next();
+            if (!ok) break;
+          }
+          const int fv = fK + 2 * j + 1, fk1 = fK + 2 * j + 2;
+          // V_j first (PV_0(j) reads it); K_(j+1) only once PV_0(j) is
+          // issued, so that the wait is off the path from the softmax's
+          // arrival to the next PV
+          if (!wait_bar_warp<kSleepMmaNs>(bar(L::KV_FULL + slot_of(fv)), par_of(fv), ctl)) { ok = false; break; }
+          if (j < cur.nT0) {  // PV_0(j), then QK_0 over P_0(j)
+            if (!wait_bar_warp<kSleepMmaNs>(bar(L::PV_READY + 0), n_pv0 & 1, ctl)) { ok = false; break; }
+            if (j == 0 && n_o0 > 0 && !wait_bar_warp<kSleepMmaNs>(bar(L::O_FREE + 0), (n_o0 - 1) & 1, ctl)) {
+              ok = false;
+              break;
+            }
+            ++n_pv0;
+            tc_fence_after();
+            pv(0, fv, j > 0);
+          }
+          if (!last && !wait_bar_warp<kSleepMmaNs>(bar(L::KV_FULL + slot_of(fk1)), par_of(fk1), ctl)) {
+            ok = false;
+            break;
+          }
+          if (!last) {
+            if (j + 1 < cur.nT0) qk(0, fk1, j + 2 == cur.nT0);
+          } else if (has_next) {
+            if (!wait_bar_warp<kSleepMmaNs>(bar(L::Q_FULL + 0), (kq + 1) & 1, ctl)) { ok = false; break; }
+            if (nxt.nT1 > 0 && !wait_bar_warp<kSleepMmaNs>(bar(L::KV_FULL + slot_of(fN)), par_of(fN), ctl)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            if (nxt.nT0 > 0) qk(0, fN, nxt.nT0 == 1); else umma_commit(bar(L::Q_EMPTY + 0));
+          }
+          // PV_1(j), then QK_1 over P_1(j)
+          if (!wait_bar_warp<kSleepMmaNs>(bar(L::PV_READY + 1), n_pv1 & 1, ctl)) { ok = false; break; }
+          if (j == 0 && n_o1 > 0 && !wait_bar_warp<kSleepMmaNs>(bar(L::O_FREE + 1), (n_o1 - 1) & 1, ctl)) {
+            ok = false;
+            break;
+          }
+          ++n_pv1;
+          tc_fence_after();
+          pv(1, fv, j > 0);
+          umma_commit(bar(L::KV_EMPTY + slot_of(fv)));
+          if (!last) {
+            qk(1, fk1, j + 2 == cur.nT1);
+            umma_commit(bar(L::KV_EMPTY + slot_of(fk1)));
+          } else if (has_next) {
+            if (!wait_bar_warp<kSleepMmaNs>(bar(L::Q_FULL + 1), (kq + 1) & 1, ctl)) { ok = false; break; }
+            tc_fence_after();
+            if (nxt.nT1 > 0) {
+              qk(1, fN, nxt.nT1 == 1);
+              umma_commit(bar(L::KV_EMPTY + slot_of(fN)));
+            } else {
+              umma_commit(bar(L::Q_EMPTY + 1));
+            }
+          }
+        }
+        if (ok) take_next();  // an item without key tiles
+        if (!ok || !has_next) break;
+        if (cur.nT0 > 0) ++n_o0;
+        if (cur.nT1 > 0) ++n_o1;
+        if (cur.nT1 == 0) ok = begin(nxt, kq + 1, fN);  // no tile above began it
+        ++kq;
+        cur = nxt;
+        fK = fN;
       }
       if (issued) {  // every MMA issued so far completes before TMEM is freed
         umma_commit(bar(L::DRAIN));
@@ -545,40 +707,72 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 13) {
     // ============================== TMA producer =============================
+    // Per item: Q_0, K_0, Q_1, V_0, then K_j V_j.  The Q of the next item
+    // waits for the current item's last QK on that stage, the K/V ring for
+    // the tiles of the previous round of the ring.
     if (lane == 0) {
-#pragma unroll
-      for (int s = 0; s < 2; ++s) {
-        mbar_arrive_expect_tx(bar(L::Q_FULL + s), L::kQBytes);
-#pragma unroll
-        for (int box = 0; box < D / 64; ++box)
-          tma_load_3d(sQ + static_cast<uint32_t>(s * L::kQBytes + box * L::kBox), &tmQ,
-                      bar(L::Q_FULL + s), box * 64, row0 + s * kBM, bh);
-      }
       int fill = 0;
       int last_fill[L::kSlots];
 #pragma unroll
       for (int i = 0; i < L::kSlots; ++i) last_fill[i] = -1;
+      int nq[2] = {0, 0};  // Q loads issued per stage
       bool ok = true;
-#pragma unroll 1
-      for (int j = 0; ok && j < n_kv; ++j) {
-#pragma unroll 1
-        for (int kv = 0; kv < 2; ++kv, ++fill) {
-          const int slot = fill % L::kSlots;
-          const uint32_t par = static_cast<uint32_t>(((fill / L::kSlots) & 1) ^ 1);
-          if (!wait_bar(bar(L::KV_EMPTY + slot), par, ctl)) { ok = false; break; }
-          if (p.test_stall && fill == 2) continue;  // test hook: withhold K_1
-          mbar_arrive_expect_tx(bar(L::KV_FULL + slot), L::kKVBytes);
-          const CUtensorMap* tm = kv == 0 ? &tmK : &tmV;
+      auto load_q = [&](const Item& it, int s) -> bool {
+        if (nq[s] > 0 && !wait_bar<kSleepProducerNs>(bar(L::Q_EMPTY + s), (nq[s] - 1) & 1, ctl)) return false;
+        mbar_arrive_expect_tx(bar(L::Q_FULL + s), L::kQBytes);
 #pragma unroll
-          for (int box = 0; box < D / 64; ++box)
-            tma_load_3d(sKV + static_cast<uint32_t>(slot * L::kKVBytes + box * L::kBox), tm,
-                        bar(L::KV_FULL + slot), box * 64, j * kBN, bh);
-          last_fill[slot] = fill;
+        for (int box = 0; box < D / 64; ++box)
+          tma_load_3d(sQ + static_cast<uint32_t>(s * L::kQBytes + box * L::kBox), &tmQ,
+                      bar(L::Q_FULL + s), box * 64, it.row0 + s * kBM, it.bh);
+        ++nq[s];
+        return true;
+      };
+      auto load_kv = [&](const Item& it, int kv, int j) -> bool {
+        const int slot = fill % L::kSlots;
+        const uint32_t par = static_cast<uint32_t>(((fill / L::kSlots) & 1) ^ 1);
+        if (!wait_bar<kSleepProducerNs>(bar(L::KV_EMPTY + slot), par, ctl)) return false;
+        if (p.test_stall && fill == 2) {  // test hook: withhold the first item's K_1
+          ++fill;
+          return true;
         }
+        mbar_arrive_expect_tx(bar(L::KV_FULL + slot), L::kKVBytes);
+        const CUtensorMap* tm = kv == 0 ? &tmK : &tmV;
+#pragma unroll
+        for (int box = 0; box < D / 64; ++box)
+          tma_load_3d(sKV + static_cast<uint32_t>(slot * L::kKVBytes + box * L::kBox), tm,
+                      bar(L::KV_FULL + slot), box * 64, j * kBN, it.bh);
+        last_fill[slot] = fill;
+        ++fill;
+        return true;
+      };
+      int idx = static_cast<int>(blockIdx.x);  // the grid never exceeds the items
+#pragma unroll 1
+      for (uint32_t k = 0; ok; ++k) {
+        // publish item k (or the end) once every role has taken item k - 4
+        const uint32_t slot = k % kItemRing;
+        if (k >= kItemRing &&
+            !wait_bar<kSleepProducerNs>(bar(L::ITEM_EMPTY + slot), (k / kItemRing - 1) & 1, ctl)) {
+          ok = false;
+          break;
+        }
+        item_ring[slot] = idx;
+        mbar_arrive(bar(L::ITEM_FULL + slot));
+        if (idx < 0) break;
+        const Item it = get_item(p, idx);
+        ok = load_q(it, 0);
+#pragma unroll 1
+        for (int j = 0; ok && j < it.nT1; ++j) {
+          ok = load_kv(it, 0, j);
+          if (ok && j == 0) ok = load_q(it, 1);
+          if (ok) ok = load_kv(it, 1, j);
+        }
+        if (ok && it.nT1 == 0) ok = load_q(it, 1);
+        idx = claim_item(p);
       }
       // drain: every load issued lands before shared memory goes away
-      wait_drain(bar(L::Q_FULL + 0), 0, p.timeout_ns);
-      wait_drain(bar(L::Q_FULL + 1), 0, p.timeout_ns);
+#pragma unroll
+      for (int s = 0; s < 2; ++s)
+        if (nq[s] > 0) wait_drain(bar(L::Q_FULL + s), (nq[s] - 1) & 1, p.timeout_ns);
 #pragma unroll 1
       for (int i = 0; i < L::kSlots; ++i)
         if (last_fill[i] >= 0)
@@ -594,6 +788,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 12) {
     tc_fence_after();
     tmem_dealloc(tmem, L::kTmemCols);
+  }
+  if (threadIdx.x == 0) {
+    // the launch's last CTA clears the scheduler slot (claims are over: a
+    // CTA claims only from its producer, which has finished)
+    __threadfence();
+    if (atomicAdd(&p.sched[1], 1ull) == gridDim.x - 1) {
+      p.sched[0] = 0ull;
+      p.sched[1] = 0ull;
+      __threadfence();
+    }
   }
 }
 

@@ -61,9 +61,9 @@ typedef enum {
 } fa_status_t;
 
 /* fa_fwd_ex flags */
-#define FA_FLAG_NO_LPT 0x1u          /* causal: plain CTA order instead of
-                                        heaviest-first (results are bitwise
-                                        identical either way)              */
+#define FA_FLAG_NO_LPT 0x1u          /* causal: items in plain order instead
+                                        of heaviest-first (results are
+                                        bitwise identical either way)      */
 #define FA_FLAG_ALWAYS_RESCALE 0x2u  /* rescale O on every key tile, not only
                                         when the row max changes (bitwise
                                         identical either way)              */
@@ -74,14 +74,19 @@ typedef enum {
                                         more than 8 in log2 units; both are
                                         exact after the final division by
                                         the row sum                         */
-#define FA_FLAG_TEST_STALL 0x100u    /* test hook: the K/V producer withholds
-                                        its second tile, so the consumers'
-                                        bounded waits run out and the kernel
-                                        reports FA_ERR_TIMEOUT             */
+#define FA_FLAG_TEST_STALL 0x100u    /* test hook: the K/V producer of every
+                                        CTA withholds its first item's second
+                                        K tile, so the consumers' bounded
+                                        waits run out and the kernel reports
+                                        FA_ERR_TIMEOUT                      */
 
 /*
  * fa_fwd -- the whole forward pass for one batch, on `stream`.
- * Prefill (Sq > 1): one fused kernel.  Decode (Sq == 1): split-KV kernel plus
+ * Prefill (Sq > 1): one fused, persistent kernel (one CTA per SM); its CTAs
+ * claim work items from a counter in a small static device array of the
+ * library (1024 slots of 16 bytes, one per launch in turn, cleared by each
+ * launch's last CTA), so two prefill launches whose GPU work overlaps must
+ * be fewer than 1024 calls apart.  Decode (Sq == 1): split-KV kernel plus
  * combine kernel, using a workspace that the library allocates on the first
  * decode call on each device and keeps until process exit (use fa_fwd_ex to
  * supply your own).
