@@ -637,12 +637,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
           }
           const int fv = fK + 2 * j + 1, fk1 = fK + 2 * j + 2;
-          // V_j first (PV_0(j) reads it); K_(j+1) only once PV_0(j) is
-          // issued, so that the wait is off the path from the softmax's
-          // arrival to the next PV
-          if (!wait_bar_warp<kSleepMmaNs>(bar(L::KV_FULL + slot_of(fv)), par_of(fv), ctl)) { ok = false; break; }
+          // V_j and PV_READY_0 first, probed together (usually both are
+          // complete; the bounded waits only when one is not); K_(j+1) only
+          // once PV_0(j) is issued, so that its wait is off the path from
+          // the softmax's arrival to the next PV
+          bool rdy = mbar_try_wait(bar(L::KV_FULL + slot_of(fv)), par_of(fv));
+          if (j < cur.nT0) rdy &= mbar_try_wait(bar(L::PV_READY + 0), n_pv0 & 1);
+          if (!__all_sync(0xffffffffu, rdy)) {
+            if (!wait_bar_warp<kSleepMmaNs>(bar(L::KV_FULL + slot_of(fv)), par_of(fv), ctl)) { ok = false; break; }
+            if (j < cur.nT0 && !wait_bar_warp<kSleepMmaNs>(bar(L::PV_READY + 0), n_pv0 & 1, ctl)) { ok = false; break; }
+          }
           if (j < cur.nT0) {  // PV_0(j), then QK_0 over P_0(j)
-            if (!wait_bar_warp<kSleepMmaNs>(bar(L::PV_READY + 0), n_pv0 & 1, ctl)) { ok = false; break; }
             if (j == 0 && n_o0 > 0 && !wait_bar_warp<kSleepMmaNs>(bar(L::O_FREE + 0), (n_o0 - 1) & 1, ctl)) {
               ok = false;
               break;
