@@ -363,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         uint32_t sr[8][16];
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc) tmem_ld16(tS + cc * 16, sr[cc]);
+        for (int cc = 0; cc < 8; cc += 2) tmem_ld32(tS + cc * 16, sr[cc], sr[cc + 1]);
         tmem_wait_ld();
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) reg_fence16(sr[cc]);
