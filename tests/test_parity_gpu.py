@@ -52,6 +52,42 @@ def test_edge_shapes(case):
     _assert(run_and_check(B, H, Sq, Skv, D, dt, causal, 11, qk_mult=2.0))
 
 
+# More work items than SMs, so every persistent CTA takes several in turn:
+# items without a visible key (causal, Sq > Skv) between others, stages with
+# no key tile, many short ragged items, LPT order.
+PERSISTENT = [  # B, H, Sq, Skv, D, dtype, causal
+    (1, 64, 1024, 128, 128, "bf16", True),
+    (4, 48, 600, 129, 128, "bf16", True),
+    (8, 32, 300, 300, 64, "fp16", True),
+    (8, 32, 300, 300, 128, "bf16", False),
+]
+
+
+@pytest.mark.parametrize("case", PERSISTENT, ids=lambda c: "x".join(map(str, c)))
+def test_persistent_item_sequences(case):
+    B, H, Sq, Skv, D, dt, causal = case
+    _assert(run_and_check(B, H, Sq, Skv, D, dt, causal, 13))
+
+
+def test_scheduler_slots_wrap_around():
+    """1100 launches, more than the 1024 scheduler slots: every launch still
+    claims every item (outputs cleared before every 100th launch must come
+    back bit for bit)."""
+    q, k, v = inputs.make_qkv(4, 64, 512, 512, 128, "bf16", 3)
+    dq, dk, dv = (t.cuda() for t in (q, k, v))
+    ref, lref = fa.fa_fwd(dq, dk, dv, causal=True)
+    o, lse = torch.empty_like(ref), torch.empty_like(lref)
+    for i in range(1100):
+        if i % 100 == 99:
+            o.zero_()
+            lse.fill_(float("nan"))
+        fa.fa_fwd(dq, dk, dv, causal=True, out=o, lse=lse)
+        if i % 100 == 99:
+            torch.cuda.synchronize()
+            assert torch.equal(o, ref) and torch.equal(lse, lref), i
+    assert fa.fa_get_device_status() == fa.FA_OK
+
+
 def test_headline_sampled_rows():
     """B4 H16 S4096 D128 bf16 non-causal at full size, in the launch the bench
     times (fa_fwd, default options); >= 512 sampled rows covering every head."""
