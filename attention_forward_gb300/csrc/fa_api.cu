@@ -10,6 +10,7 @@
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <vector>
 
 #include "../../include/fa.h"
 #include "fa_internal.h"
@@ -69,8 +70,14 @@ struct DeviceState {
   unsigned long long* sched = nullptr;  // g_sched on this device
   bool regs_ok[2][2] = {};  // [D==128][bf16]
   bool regs_checked[2][2] = {};
-  void* workspace = nullptr;  // fa_fwd's cached decode workspace
-  size_t workspace_bytes = 0;
+  // fa_fwd's workspaces for split partials, one per stream (calls on one
+  // stream run in order; calls on different streams may overlap)
+  struct StreamWorkspace {
+    cudaStream_t stream;
+    void* ptr;
+    size_t bytes;
+  };
+  std::vector<StreamWorkspace> workspaces;
 };
 
 std::mutex g_mu;
@@ -164,9 +171,67 @@ fa_status_t encode_3d(CUtensorMap* m, const void* base, int D, int S, int BH,
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+// fa_fwd's workspace for `stream` on this device, grown to `need` bytes.
+fa_status_t stream_workspace(DeviceState& d, cudaStream_t stream, size_t need, void** out) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  for (auto& w : d.workspaces) {
+    if (w.stream != stream) continue;
+    if (w.bytes < need) {
+      cudaFree(w.ptr);  // waits for the work that used it
+      w.ptr = nullptr;
+      w.bytes = 0;
+      if (cudaMalloc(&w.ptr, need) != cudaSuccess) return FA_ERR_CUDA;
+      w.bytes = need;
+    }
+    *out = w.ptr;
+    return FA_OK;
+  }
+  void* ptr = nullptr;
+  if (cudaMalloc(&ptr, need) != cudaSuccess) return FA_ERR_CUDA;
+  d.workspaces.push_back({stream, ptr, need});
+  *out = ptr;
+  return FA_OK;
+}
+
+// Prefill key splits: only when the (query tile, head) items are fewer than
+// the SMs.  Picks the split count with the smallest estimated time, counted
+// in key tiles: rounds of one item per SM times the tiles of a range, plus
+// eight tiles for the combine kernel and the fp32 partials when split (on
+// GB300 a 1024-key item split in two measured slower than unsplit); ties go
+// to fewer splits.  An explicit num_splits >= 1 is taken as is (capped at
+// the key tiles).
+int prefill_splits(int BH, int Sq, int Skv, int sm_count, int num_splits) {
+  const long long n_base = static_cast<long long>((Sq + fa::kRowsPerCta - 1) / fa::kRowsPerCta) * BH;
+  const int n_tiles = (Skv + fa::kBN - 1) / fa::kBN;
+  if (num_splits >= 1) return std::min(num_splits, n_tiles);
+  const long long sms = sm_count > 0 ? sm_count : 148;
+  if (n_base >= sms) return 1;
+  constexpr long long kCombineTiles = 8;
+  int best = 1;
+  long long best_cost = n_tiles;
+  for (int s = 2; s <= std::min(n_tiles, 64); ++s) {
+    const int tps = (n_tiles + s - 1) / s;
+    const int s_eff = (n_tiles + tps - 1) / tps;
+    const long long rounds = (n_base * s_eff + sms - 1) / sms;
+    const long long cost = rounds * tps + kCombineTiles;
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = s_eff;
+    }
+  }
+  return best;
+}
+
+size_t prefill_ws_bytes(int BH, int Sq, int D, int n_splits) {
+  if (n_splits <= 1) return 0;
+  const size_t rows = static_cast<size_t>(n_splits) * BH * Sq;
+  return ((rows * D * sizeof(float) + 255) / 256) * 256 + ((rows * sizeof(float) + 255) / 256) * 256;
+}
+
 fa_status_t run_prefill(DeviceState& d, const void* q, const void* k, const void* v,
                         void* o, float* lse, int B, int H, int Sq, int Skv, int D,
                         float scale, int causal, bool bf16, unsigned flags,
+                        int num_splits, void* ws, size_t ws_bytes, bool own_ws,
                         cudaStream_t stream) {
   fa_status_t st = get_encoder();
   if (st != FA_OK) return st;
@@ -202,7 +267,32 @@ fa_status_t run_prefill(DeviceState& d, const void* q, const void* k, const void
   p.test_stall = (flags & FA_FLAG_TEST_STALL) ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.rescale_tau = (flags & FA_FLAG_EXACT_MAX) ? 0.f : 8.f;
-  const long long n_items = static_cast<long long>(p.n_qtiles) * BH;
+  const int n_tiles = (Skv + fa::kBN - 1) / fa::kBN;
+  int n_splits = prefill_splits(BH, Sq, Skv, d.sm_count, num_splits);
+  if (n_splits > 1 && static_cast<long long>(BH) * Sq > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  p.tiles_per_split = (n_tiles + n_splits - 1) / n_splits;
+  n_splits = (n_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
+  size_t need = prefill_ws_bytes(BH, Sq, D, n_splits);
+  if (need > 0 && !own_ws && num_splits == 0 &&
+      (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u))) {
+    // the library's choice, without room for the partials: no split
+    n_splits = 1;
+    p.tiles_per_split = n_tiles;
+    need = 0;
+  }
+  p.n_splits = n_splits;
+  if (need > 0) {
+    if (own_ws) {
+      if ((st = stream_workspace(d, stream, need, &ws)) != FA_OK) return st;
+    } else if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u)) {
+      return FA_ERR_WORKSPACE;
+    }
+    const size_t rows = static_cast<size_t>(n_splits) * BH * Sq;
+    p.part_o = static_cast<float*>(ws);
+    p.part_lse = reinterpret_cast<float*>(static_cast<char*>(ws) +
+                                          ((rows * D * sizeof(float) + 255) / 256) * 256);
+  }
+  const long long n_items = static_cast<long long>(p.n_qtiles) * BH * n_splits;
   if (n_items > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
   p.n_items = static_cast<int>(n_items);
   p.sched = d.sched + 2 * (g_launch_seq.fetch_add(1) % fa::kSchedSlots);
@@ -210,6 +300,18 @@ fa_status_t run_prefill(DeviceState& d, const void* q, const void* k, const void
   const int grid = static_cast<int>(std::min<long long>(n_items, d.sm_count > 0 ? d.sm_count : 1));
   if (fa::launch_prefill(D, bf16, tq, tk, tv, to, p, grid, stream) != cudaSuccess)
     return FA_ERR_CUDA;
+  if (n_splits > 1) {
+    // merge the key ranges of every (head, query row): the decode combine
+    // over BH * Sq rows
+    fa::DecodeParams c{};
+    c.o = o;
+    c.lse = lse;
+    c.part_o = p.part_o;
+    c.part_lse = p.part_lse;
+    c.BH = BH * Sq;
+    c.n_splits = n_splits;
+    if (fa::launch_decode_combine(D, bf16, c, stream) != cudaSuccess) return FA_ERR_CUDA;
+  }
   return FA_OK;
 }
 
@@ -247,15 +349,8 @@ fa_status_t run_decode(DeviceState& d, const void* q, const void* k, const void*
   const size_t need = decode_ws_bytes(BH, n_splits, D);
   if (need > 0) {
     if (own_ws) {
-      std::lock_guard<std::mutex> lock(g_mu);
-      if (d.workspace_bytes < need) {
-        if (d.workspace) cudaFree(d.workspace);
-        d.workspace = nullptr;
-        d.workspace_bytes = 0;
-        if (cudaMalloc(&d.workspace, need) != cudaSuccess) return FA_ERR_CUDA;
-        d.workspace_bytes = need;
-      }
-      ws = d.workspace;
+      const fa_status_t wst = stream_workspace(d, stream, need, &ws);
+      if (wst != FA_OK) return wst;
     } else {
       if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u))
         return FA_ERR_WORKSPACE;
@@ -304,7 +399,7 @@ fa_status_t forward(const void* q, const void* k, const void* v, void* o, float*
     return run_decode(*d, q, k, v, o, lse, B * H, Skv, D, scale, bf16, num_splits, ws,
                       ws_bytes, own_ws, stream);
   return run_prefill(*d, q, k, v, o, lse, B, H, Sq, Skv, D, scale, causal, bf16, flags,
-                     stream);
+                     num_splits, ws, ws_bytes, own_ws, stream);
 }
 
 }  // namespace
@@ -319,12 +414,18 @@ fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* 
 }
 
 size_t fa_workspace_bytes(int B, int H, int Sq, int Skv, int D, int num_splits) {
-  if (B < 1 || H < 1 || Sq != 1 || Skv < 1 || (D != 64 && D != 128) || num_splits < 0)
+  if (B < 1 || H < 1 || Sq < 1 || Skv < 1 || (D != 64 && D != 128) || num_splits < 0)
     return 0;
   int sms = 0;
   if (num_splits == 0) {
     DeviceState* d = nullptr;
     if (current_device(&d, nullptr) == FA_OK) sms = d->sm_count;
+  }
+  if (Sq > 1) {
+    const int n_tiles = (Skv + fa::kBN - 1) / fa::kBN;
+    const int s = prefill_splits(B * H, Sq, Skv, sms, num_splits);
+    const int tps = (n_tiles + s - 1) / s;
+    return prefill_ws_bytes(B * H, Sq, D, (n_tiles + tps - 1) / tps);
   }
   const int kps = decode_keys_per_split(B * H, Skv, sms, num_splits);
   return decode_ws_bytes(B * H, (Skv + kps - 1) / kps, D);

@@ -33,13 +33,19 @@ struct PrefillParams {
   int BH;                     // B*H
   int Sq, Skv;
   int n_qtiles;               // ceil(Sq / kRowsPerCta)
-  int n_items;                // n_qtiles * BH work items (256 rows of one head)
+  int n_items;                // n_qtiles * BH * n_splits work items
   int causal;
   int lpt;                    // heaviest-first item order (causal only)
   int always_rescale;
   int test_stall;
   float scale_log2;           // scale * log2(e)
   float rescale_tau;          // raise the reference max only past this (log2)
+  // split keys (kept after the fields above: the kernel with the whole key
+  // range measured about 1% slower with these inserted among them)
+  int n_splits;               // key ranges per (query tile, head); 1: no split
+  int tiles_per_split;        // key tiles of kBN per range
+  float* part_o;              // n_splits > 1: [n_splits, BH*Sq, D] fp32, O / l
+  float* part_lse;            // n_splits > 1: [n_splits, BH*Sq] fp32
 };
 
 // Decode (Sq == 1) split-KV.

@@ -109,9 +109,17 @@ struct PrefillLayout {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-// One work item: 256 query rows (two stages) of one (batch, head).
-struct Item {
+// One work item: 256 query rows (two stages) of one (batch, head), over the
+// key tiles [t0, t0 + nT1): all of them, unless the keys are split into
+// ranges (then `split` numbers the range).
+template <bool kSplit>
+struct ItemT {
   int bh, row0, nT0, nT1;
+  static constexpr int t0 = 0, split = 0;
+};
+template <>
+struct ItemT<true> {
+  int bh, row0, nT0, nT1, t0, split;
 };
 
 // Register split between warpgroups (setmaxnreg): softmax warpgroups get
@@ -219,20 +227,33 @@ __device__ __forceinline__ int stage_tiles(int row_first, int Sq, int Skv,
   return min(n_all, last_key / kBN + 1);
 }
 
-// Item idx (0 <= idx < n_items): heaviest first under causal LPT.
-__device__ __forceinline__ Item get_item(const PrefillParams& p, int idx) {
-  Item it;
+// Item idx (0 <= idx < n_items): heaviest first under causal LPT; with
+// split keys, the key ranges of one query tile are consecutive items.
+template <bool kSplit>
+__device__ __forceinline__ ItemT<kSplit> get_item(const PrefillParams& p, int idx) {
+  ItemT<kSplit> it;
+  int qi = idx;
+  if constexpr (kSplit) {
+    qi = idx / p.n_splits;
+    it.split = idx - qi * p.n_splits;
+  }
   int qtile;
   if (p.causal && p.lpt) {
-    qtile = p.n_qtiles - 1 - idx / p.BH;
-    it.bh = idx % p.BH;
+    qtile = p.n_qtiles - 1 - qi / p.BH;
+    it.bh = qi % p.BH;
   } else {
-    qtile = idx % p.n_qtiles;
-    it.bh = idx / p.n_qtiles;
+    qtile = qi % p.n_qtiles;
+    it.bh = qi / p.n_qtiles;
   }
   it.row0 = qtile * kRowsPerCta;
   it.nT0 = stage_tiles(it.row0, p.Sq, p.Skv, p.causal);
   it.nT1 = stage_tiles(it.row0 + kBM, p.Sq, p.Skv, p.causal);
+  if constexpr (kSplit) {
+    it.t0 = it.split * p.tiles_per_split;
+    const int t1 = it.t0 + p.tiles_per_split;
+    it.nT0 = max(0, min(it.nT0, t1) - it.t0);
+    it.nT1 = max(0, min(it.nT1, t1) - it.t0);
+  }
   return it;
 }
 
@@ -260,7 +281,7 @@ __device__ __forceinline__ int take_item(const volatile int* ring, uint32_t full
   return idx;
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_prefill_kernel(const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmK,
@@ -350,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (uint32_t k = 0; ok; ++k) {
       const int idx = take_item<0>(item_ring, bar(L::ITEM_FULL), bar(L::ITEM_EMPTY), k, ctl, ok);
       if (!ok || idx < 0) break;
-      const Item it = get_item(p, idx);
+      const ItemT<kSplit> it = get_item<kSplit>(p, idx);
       const int nT = s == 0 ? it.nT0 : it.nT1;
       const int stage_row0 = it.row0 + s * kBM;
       const int row_g = stage_row0 + r;        // query row
@@ -369,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int cc = 0; cc < 8; ++cc) reg_fence16(sr[cc]);
 
         // mask: ragged key tail, and the causal diagonal
-        const int key0 = j * kBN;
+        const int key0 = (it.t0 + j) * kBN;
         const bool need_mask =
             (key0 + kBN > p.Skv) || (p.causal && key0 + kBN - 1 > stage_row0 + off);
         if (need_mask) {
@@ -454,7 +475,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // once the item's last PV_s has completed (then O_s is final)
       if (row_g < p.Sq) {
         const float lse = l > 0.f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
-        p.lse[static_cast<size_t>(it.bh) * p.Sq + row_g] = lse;
+        if constexpr (kSplit)
+          p.part_lse[(static_cast<size_t>(it.split) * p.BH + it.bh) * p.Sq + row_g] = lse;
+        else
+          p.lse[static_cast<size_t>(it.bh) * p.Sq + row_g] = lse;
       }
       if (nT > 0) {
         if (!wait_bar_warp(bar(L::O_READY + s), (n_s - 1) & 1, ctl)) { ok = false; break; }
@@ -482,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int idx = take_item<kSleepEpilogueNs>(item_ring, bar(L::ITEM_FULL),
                                                   bar(L::ITEM_EMPTY), k, ctl, ok);
       if (!ok || idx < 0) break;
-      const Item it = get_item(p, idx);
+      const ItemT<kSplit> it = get_item<kSplit>(p, idx);
 #pragma unroll
       for (int s = 0; s < 2; ++s) {
         if (!ok) continue;
@@ -499,10 +523,43 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait_bar_warp<kSleepEpilogueNs>(bar(L::O_READY + s), (n_t - 1) & 1, ctl)) { ok = false; continue; }
           tc_fence_after();
         }
+        const uint32_t tO = tmem + t_lane + static_cast<uint32_t>(L::kTmemO + s * D);
+        if constexpr (kSplit) {
+          // a key range: O / l of this range in fp32, one row per thread
+          const int row_g = it.row0 + s * kBM + r;
+          float4* prow = reinterpret_cast<float4*>(
+              p.part_o + ((static_cast<size_t>(it.split) * p.BH + it.bh) * p.Sq +
+                          static_cast<size_t>(row_g)) * D);
+#pragma unroll 1
+          for (int cc = 0; cc < D / 16; ++cc) {
+            uint32_t v[16];
+            if (have_o) {
+              tmem_ld16(tO + cc * 16, v);
+              tmem_wait_ld();
+              reg_fence16(v);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) v[e] = 0u;
+            }
+            if (row_g < p.Sq) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                prow[cc * 4 + e] = make_float4(__uint_as_float(v[4 * e]) * inv_l,
+                                               __uint_as_float(v[4 * e + 1]) * inv_l,
+                                               __uint_as_float(v[4 * e + 2]) * inv_l,
+                                               __uint_as_float(v[4 * e + 3]) * inv_l);
+            }
+          }
+          if (have_o) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(L::O_FREE + s));
+          }
+          continue;
+        }
         // the slice is free once the previous store has read it
         if (lane == 0) bulk_wait_group_read0();
         __syncwarp();
-        const uint32_t tO = tmem + t_lane + static_cast<uint32_t>(L::kTmemO + s * D);
 #pragma unroll 1
         for (int cc = 0; cc < D / 16; ++cc) {
           uint32_t v[16];
@@ -582,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // First QKs of an item whose Q is in buffer phase kq and whose K_0 is
       // fill f (used for the CTA's first item and after an item without keys)
-      auto begin = [&](const Item& it, int kq, int f) -> bool {
+      auto begin = [&](const ItemT<kSplit>& it, int kq, int f) -> bool {
         if (!wait_bar_warp<kSleepMmaNs>(bar(L::Q_FULL + 0), kq & 1, ctl) ||
             !wait_bar_warp<kSleepMmaNs>(bar(L::Q_FULL + 1), kq & 1, ctl))
           return false;
@@ -611,7 +668,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       const int first = take_item<kSleepMmaNs>(item_ring, bar(L::ITEM_FULL),
                                                bar(L::ITEM_EMPTY), 0, ctl, ok);
-      Item cur = first >= 0 ? get_item(p, first) : Item{0, 0, 0, 0};
+      ItemT<kSplit> cur = first >= 0 ? get_item<kSplit>(p, first) : ItemT<kSplit>{0, 0, 0, 0};
       if (ok && first >= 0) ok = begin(cur, 0, 0);
       else ok = false;
 #pragma unroll 1
@@ -619,14 +676,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the next item is taken at this item's last key tile, once the
         // producer has claimed it (it does so after the last K/V fill)
         bool taken = false, has_next = false;
-        Item nxt{0, 0, 0, 0};
+        ItemT<kSplit> nxt{0, 0, 0, 0};
         auto take_next = [&]() {
           if (taken) return;
           taken = true;
           const int nidx = take_item<kSleepMmaNs>(item_ring, bar(L::ITEM_FULL),
                                                   bar(L::ITEM_EMPTY), kq + 1, ctl, ok);
           has_next = ok && nidx >= 0;
-          if (has_next) nxt = get_item(p, nidx);
+          if (has_next) nxt = get_item<kSplit>(p, nidx);
         };
         const int fN = fK + 2 * cur.nT1;  // the next item's K_0
 #pragma unroll 1
@@ -722,7 +779,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < L::kSlots; ++i) last_fill[i] = -1;
       int nq[2] = {0, 0};  // Q loads issued per stage
       bool ok = true;
-      auto load_q = [&](const Item& it, int s) -> bool {
+      auto load_q = [&](const ItemT<kSplit>& it, int s) -> bool {
         if (nq[s] > 0 && !wait_bar<kSleepProducerNs>(bar(L::Q_EMPTY + s), (nq[s] - 1) & 1, ctl)) return false;
         mbar_arrive_expect_tx(bar(L::Q_FULL + s), L::kQBytes);
 #pragma unroll
@@ -732,7 +789,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++nq[s];
         return true;
       };
-      auto load_kv = [&](const Item& it, int kv, int j) -> bool {
+      auto load_kv = [&](const ItemT<kSplit>& it, int kv, int j) -> bool {
         const int slot = fill % L::kSlots;
         const uint32_t par = static_cast<uint32_t>(((fill / L::kSlots) & 1) ^ 1);
         if (!wait_bar<kSleepProducerNs>(bar(L::KV_EMPTY + slot), par, ctl)) return false;
@@ -745,7 +802,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int box = 0; box < D / 64; ++box)
           tma_load_3d(sKV + static_cast<uint32_t>(slot * L::kKVBytes + box * L::kBox), tm,
-                      bar(L::KV_FULL + slot), box * 64, j * kBN, it.bh);
+                      bar(L::KV_FULL + slot), box * 64, (it.t0 + j) * kBN, it.bh);
         last_fill[slot] = fill;
         ++fill;
         return true;
@@ -763,7 +820,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         item_ring[slot] = idx;
         mbar_arrive(bar(L::ITEM_FULL + slot));
         if (idx < 0) break;
-        const Item it = get_item(p, idx);
+        const ItemT<kSplit> it = get_item<kSplit>(p, idx);
         ok = load_q(it, 0);
 #pragma unroll 1
         for (int j = 0; ok && j < it.nT1; ++j) {

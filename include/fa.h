@@ -86,10 +86,13 @@ typedef enum {
  * claim work items from a counter in a small static device array of the
  * library (1024 slots of 16 bytes, one per launch in turn, cleared by each
  * launch's last CTA), so two prefill launches whose GPU work overlaps must
- * be fewer than 1024 calls apart.  Decode (Sq == 1): split-KV kernel plus
- * combine kernel, using a workspace that the library allocates on the first
- * decode call on each device and keeps until process exit (use fa_fwd_ex to
- * supply your own).
+ * be fewer than 1024 calls apart.  When the (256-row query tile, head)
+ * items are fewer than the SMs (short query blocks, few heads), the keys of
+ * each item are split into ranges whose fp32 partials a combine kernel
+ * merges.  Decode (Sq == 1): split-KV kernel plus combine kernel.  The
+ * partials go to a workspace that the library allocates on the first call
+ * that needs one on each device and keeps until process exit (use fa_fwd_ex
+ * to supply your own).
  * Returns FA_OK once the work is enqueued.
  */
 fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o,
@@ -99,10 +102,12 @@ fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o,
 /*
  * fa_workspace_bytes -- bytes of device workspace fa_fwd_ex needs for this
  * shape with `num_splits` key splits (0 = the library's choice); 0 when the
- * shape needs none.  The split-KV partials are fp32 (O, LSE) per split: the
- * fp32 workspace round trip that "The FA5090 Optimization Journey" section 2.7
- * measured (and rejected for prefill); here it serves only decode, where one
- * query row per head leaves too few work items to fill the GPU otherwise.
+ * shape needs none.  The split-KV partials are fp32 (O, LSE) per split and
+ * row: the fp32 workspace round trip that "The FA5090 Optimization Journey"
+ * section 2.7 measured (and rejected for prefill at its sizes).  Here the
+ * library splits only decode, where one query row per head leaves too few
+ * work items to fill the GPU, and prefill whose items are fewer than the
+ * SMs.
  */
 size_t fa_workspace_bytes(int B, int H, int Sq, int Skv, int D,
                           int num_splits);
@@ -110,7 +115,10 @@ size_t fa_workspace_bytes(int B, int H, int Sq, int Skv, int D,
 /*
  * fa_fwd_ex -- fa_fwd with explicit options.
  *   flags       FA_FLAG_* bits above (0 for the default path)
- *   num_splits  decode key splits; 0 = the library's choice, 1 = no split
+ *   num_splits  key splits; 0 = the library's choice, 1 = no split.  With
+ *               0, a prefill whose workspace is NULL or smaller than
+ *               fa_workspace_bytes(..., 0) runs without a split; decode
+ *               and an explicit split count need the workspace.
  *   workspace   caller-owned device memory, 256-byte aligned, at least
  *               fa_workspace_bytes(...) bytes; may be NULL when that is 0.
  *               It must not be used by anything else until the work on

@@ -69,7 +69,12 @@ def test_argument_errors_precede_any_cuda_call(lib, kw, want):
 
 def test_workspace_and_staging_sizes(lib):
     from attention_forward_gb300 import fa
-    assert fa.fa_workspace_bytes(1, 1, 128, 128, 128) == 0   # prefill: none
+    assert fa.fa_workspace_bytes(1, 1, 128, 128, 128) == 0   # one key tile: no split
+    assert fa.fa_workspace_bytes(4, 64, 4096, 4096, 128) == 0  # items fill the GPU
+    assert fa.fa_workspace_bytes(1, 8, 256, 16384, 128, 1) == 0  # no split asked
+    n = fa.fa_workspace_bytes(1, 8, 256, 16384, 128, 4)  # 4 key ranges: O and LSE
+    assert n >= 4 * 8 * 256 * (128 + 1) * 4 and n % 256 == 0
+    assert fa.fa_workspace_bytes(1, 8, 256, 16384, 128) > 0   # the library splits
     assert fa.fa_workspace_bytes(1, 1, 1, 8192, 128, 1) == 0  # one split
     n = fa.fa_workspace_bytes(2, 3, 1, 1000, 128, 4)
     per = 2 * 3 * 4

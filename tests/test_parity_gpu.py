@@ -132,12 +132,49 @@ def test_decode_splits(num_splits, D, dt, Skv):
     _assert(check(q, k, v, o, lse, False, dt))
 
 
-def test_repeat_lpt_and_rescale_switches_are_bitwise_identical():
+PREFILL_SPLITS = [  # B, H, Sq, Skv, D, dtype, causal, num_splits
+    (2, 3, 300, 1000, 128, "bf16", True, 2),
+    (2, 3, 300, 1000, 128, "bf16", False, 3),
+    (1, 2, 700, 2048, 64, "fp16", True, 5),
+    (1, 1, 600, 300, 128, "bf16", True, 3),   # some ranges see no key of a row
+    (2, 2, 257, 129, 64, "bf16", False, 2),
+]
+
+
+@pytest.mark.parametrize("case", PREFILL_SPLITS, ids=lambda c: "x".join(map(str, c)))
+def test_prefill_key_splits(case):
+    """Prefill with the keys split into ranges (fp32 partials in the caller's
+    workspace, merged by the combine kernel)."""
+    B, H, Sq, Skv, D, dt, causal, n = case
+    q, k, v = inputs.make_qkv(B, H, Sq, Skv, D, dt, 17, 2.0)
+    need = fa.fa_workspace_bytes(B, H, Sq, Skv, D, n)
+    assert need > 0
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    o, lse = run_kernel(q, k, v, causal, num_splits=n, workspace=ws)
+    _assert(check(q, k, v, o, lse, causal, dt))
+    small = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(fa.FAError) as e:
+        run_kernel(q, k, v, causal, num_splits=n, workspace=small)
+    assert e.value.status == fa.FA_ERR_WORKSPACE
+
+
+def test_prefill_few_items_long_keys():
+    """A short query block over a long context (8 items on the whole GPU):
+    fa_fwd splits the keys by itself."""
+    assert fa.fa_workspace_bytes(1, 8, 256, 16384, 128) > 0
+    _assert(run_and_check(1, 8, 256, 16384, 128, "bf16", True, 19))
+
+
+@pytest.mark.parametrize("num_splits", [1, 3])
+def test_repeat_lpt_and_rescale_switches_are_bitwise_identical(num_splits):
     q, k, v = inputs.make_qkv(2, 4, 1000, 1000, 128, "bf16", 5, 4.0)
-    o1, l1 = run_kernel(q, k, v, True)
-    o2, l2 = run_kernel(q, k, v, True)
-    o3, l3 = run_kernel(q, k, v, True, flags=fa.FA_FLAG_NO_LPT)
-    o4, l4 = run_kernel(q, k, v, True, flags=fa.FA_FLAG_ALWAYS_RESCALE)
+    need = fa.fa_workspace_bytes(2, 4, 1000, 1000, 128, num_splits)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
+    kw = dict(num_splits=num_splits, workspace=ws)
+    o1, l1 = run_kernel(q, k, v, True, **kw)
+    o2, l2 = run_kernel(q, k, v, True, **kw)
+    o3, l3 = run_kernel(q, k, v, True, flags=fa.FA_FLAG_NO_LPT, **kw)
+    o4, l4 = run_kernel(q, k, v, True, flags=fa.FA_FLAG_ALWAYS_RESCALE, **kw)
     for o, l in ((o2, l2), (o3, l3), (o4, l4)):
         assert torch.equal(o, o1) and torch.equal(l, l1)
 
