@@ -70,6 +70,10 @@ struct DeviceState {
   unsigned long long* sched = nullptr;  // g_sched on this device
   bool regs_ok[2][2] = {};  // [D==128][bf16]
   bool regs_checked[2][2] = {};
+  // the CTA-pair kernel (D = 128): register check and the number of pairs
+  // (two-CTA clusters) that fit on the device at once, per dtype
+  bool pair_checked[2] = {};
+  int pair_slots[2] = {};  // 0: not usable
   // fa_fwd's workspaces for split partials, one per stream (calls on one
   // stream run in order; calls on different streams may overlap)
   struct StreamWorkspace {
@@ -228,6 +232,65 @@ size_t prefill_ws_bytes(int BH, int Sq, int D, int n_splits) {
   return ((rows * D * sizeof(float) + 255) / 256) * 256 + ((rows * sizeof(float) + 255) / 256) * 256;
 }
 
+// The library runs prefill on CTA pairs where they measured faster than
+// single CTAs on GB300: long rows (non-causal from 4096 queries and keys,
+// causal from 16384), and at least one 512-row item per pair of SMs.
+bool pair_by_default(int BH, int Sq, int Skv, int causal, int sm_count) {
+  const long long items = static_cast<long long>(BH) * ((Sq + 511) / 512);
+  if (items < (sm_count > 0 ? sm_count / 2 : 76)) return false;
+  return causal ? Sq >= 16384 : (Sq >= 4096 && Skv >= 4096);
+}
+
+// Prefill by CTA pairs (FA_FLAG_PAIR, D = 128, whole key range): items of 512
+// query rows, a persistent grid of two-CTA clusters.
+fa_status_t run_prefill_pair(DeviceState& d, const void* q, const void* k, const void* v,
+                             void* o, float* lse, int BH, int Sq, int Skv, float scale,
+                             int causal, bool bf16, unsigned flags, cudaStream_t stream) {
+  const int ti = bf16 ? 1 : 0;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!d.pair_checked[ti]) {
+      int regs = 0, n = 0;
+      if (fa::prefill_pair_num_regs(bf16, &regs) != cudaSuccess) return FA_ERR_CUDA;
+      if (regs == 128 && fa::prefill_pair_max_pairs(bf16, &n) != cudaSuccess) return FA_ERR_CUDA;
+      d.pair_checked[ti] = true;
+      d.pair_slots[ti] = regs == 128 ? n : 0;
+    }
+    if (d.pair_slots[ti] <= 0) return FA_ERR_UNSUPPORTED;
+  }
+  constexpr int D = 128;
+  CUtensorMap tq, tk, tv, to;
+  fa_status_t st;
+  if ((st = encode_3d(&tq, q, D, Sq, BH, fa::kBM, bf16)) != FA_OK) return st;
+  if ((st = encode_3d(&tk, k, D, Skv, BH, fa::kBN / 2, bf16)) != FA_OK) return st;  // a CTA's 64 keys
+  if ((st = encode_3d(&tv, v, D, Skv, BH, fa::kBN, bf16)) != FA_OK) return st;
+  if ((st = encode_3d(&to, o, D, Sq, BH, 32, bf16)) != FA_OK) return st;
+  fa::PrefillParams p{};
+  p.lse = lse;
+  p.status = d.status;
+  p.timeout_ns = g_watchdog_ns.load();
+  p.BH = BH;
+  p.Sq = Sq;
+  p.Skv = Skv;
+  p.n_qtiles = (Sq + 511) / 512;
+  p.causal = causal ? 1 : 0;
+  p.lpt = (flags & FA_FLAG_NO_LPT) ? 0 : 1;
+  p.always_rescale = (flags & FA_FLAG_ALWAYS_RESCALE) ? 1 : 0;
+  p.test_stall = (flags & FA_FLAG_TEST_STALL) ? 1 : 0;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.rescale_tau = (flags & FA_FLAG_EXACT_MAX) ? 0.f : 8.f;
+  p.n_splits = 1;
+  p.tiles_per_split = (Skv + fa::kBN - 1) / fa::kBN;
+  const long long n_items = static_cast<long long>(p.n_qtiles) * BH;
+  if (n_items > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  p.n_items = static_cast<int>(n_items);
+  p.sched = d.sched + 2 * (g_launch_seq.fetch_add(1) % fa::kSchedSlots);
+  const int n_pairs = static_cast<int>(std::min<long long>(n_items, d.pair_slots[ti]));
+  if (fa::launch_prefill_pair(bf16, tq, tk, tv, to, p, n_pairs, stream) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return FA_OK;
+}
+
 fa_status_t run_prefill(DeviceState& d, const void* q, const void* k, const void* v,
                         void* o, float* lse, int B, int H, int Sq, int Skv, int D,
                         float scale, int causal, bool bf16, unsigned flags,
@@ -248,6 +311,10 @@ fa_status_t run_prefill(DeviceState& d, const void* q, const void* k, const void
     if (!d.regs_ok[di][ti]) return FA_ERR_UNSUPPORTED;
   }
   const int BH = B * H;
+  if (D == 128 && num_splits <= 1 && !(flags & FA_FLAG_SINGLE_CTA) &&
+      ((flags & FA_FLAG_PAIR) || pair_by_default(BH, Sq, Skv, causal, d.sm_count)))
+    return run_prefill_pair(d, q, k, v, o, lse, BH, Sq, Skv, scale, causal, bf16, flags,
+                            stream);
   CUtensorMap tq, tk, tv, to;
   if ((st = encode_3d(&tq, q, D, Sq, BH, fa::kBM, bf16)) != FA_OK) return st;
   if ((st = encode_3d(&tk, k, D, Skv, BH, fa::kBN, bf16)) != FA_OK) return st;
@@ -514,6 +581,18 @@ const char* fa_status_string(fa_status_t status) {
   return "unknown status";
 }
 
-int fa_version(void) { return 10000; }
+int fa_prefill_uses_pairs(int B, int H, int Sq, int Skv, int D, int causal, unsigned flags,
+                          int num_splits) {
+  if (B <= 0 || H <= 0 || Sq <= 1 || Skv <= 0 || D != 128 || num_splits > 1 ||
+      (flags & FA_FLAG_SINGLE_CTA))
+    return 0;
+  if (flags & FA_FLAG_PAIR) return 1;
+  int sms = 0;
+  DeviceState* d = nullptr;
+  if (current_device(&d, nullptr) == FA_OK) sms = d->sm_count;
+  return pair_by_default(B * H, Sq, Skv, causal, sms) ? 1 : 0;
+}
+
+int fa_version(void) { return 10100; }
 
 }  // extern "C"

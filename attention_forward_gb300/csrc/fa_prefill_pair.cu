@@ -1,0 +1,88 @@
+// fa_prefill_pair.cu -- instantiations and launcher of the CTA-pair prefill
+// kernel (head dimension 128, fp16 and bf16, whole key range), launched with
+// clusters of two CTAs.
+#include <mutex>
+
+#include "fa_launch.h"
+#include "fa_prefill_pair.cuh"
+
+namespace fa {
+namespace {
+
+template <bool BF16>
+cudaError_t set_attrs() {
+  static std::mutex mu;
+  static bool done[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(fa_prefill_pair_kernel<BF16>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, PairLayout::kSmemBytes);
+  if (e == cudaSuccess) done[dev] = true;
+  return e;
+}
+
+cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = PairLayout::kSmemBytes;
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+template <bool BF16>
+cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                   const CUtensorMap& o, const PrefillParams& p, int n_pairs,
+                   cudaStream_t stream) {
+  cudaError_t e = set_attrs<BF16>();
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg = pair_config(2 * n_pairs, stream, attr);
+  return cudaLaunchKernelEx(&cfg, fa_prefill_pair_kernel<BF16>, q, k, v, o, p);
+}
+
+template <bool BF16>
+cudaError_t max_pairs(int* n) {
+  cudaError_t e = set_attrs<BF16>();
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg = pair_config(2, nullptr, attr);
+  return cudaOccupancyMaxActiveClusters(n, fa_prefill_pair_kernel<BF16>, &cfg);
+}
+
+template <bool BF16>
+cudaError_t num_regs(int* regs) {
+  cudaFuncAttributes a{};
+  const cudaError_t e = cudaFuncGetAttributes(&a, fa_prefill_pair_kernel<BF16>);
+  if (e == cudaSuccess) *regs = a.numRegs;
+  return e;
+}
+
+}  // namespace
+
+cudaError_t prefill_pair_max_pairs(bool bf16, int* n) {
+  return bf16 ? max_pairs<true>(n) : max_pairs<false>(n);
+}
+
+cudaError_t prefill_pair_num_regs(bool bf16, int* regs) {
+  return bf16 ? num_regs<true>(regs) : num_regs<false>(regs);
+}
+
+cudaError_t launch_prefill_pair(bool bf16, const CUtensorMap& q, const CUtensorMap& k,
+                                const CUtensorMap& v, const CUtensorMap& o,
+                                const PrefillParams& p, int n_pairs, cudaStream_t stream) {
+  return bf16 ? launch<true>(q, k, v, o, p, n_pairs, stream)
+              : launch<false>(q, k, v, o, p, n_pairs, stream);
+}
+
+}  // namespace fa

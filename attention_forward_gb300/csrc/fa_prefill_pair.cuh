@@ -1,0 +1,723 @@
+// fa_prefill_pair.cuh -- the fused attention forward (prefill) kernel run by
+// CTA pairs: a cluster of two CTAs on two SMs whose tensor cores work as one
+// (tcgen05 .cta_group::2, M = 256).  Head dimension 128, whole key range.
+//
+// A pair item is 512 query rows of one (batch, head): two ping-pong stages of
+// 256 rows, each split between the CTAs (rank r holds rows 128*r .. 128*r+127
+// of the stage).  One MMA of the leader CTA (rank 0) computes a stage's
+// S = Q K^T for all 256 rows, with A = Q from both CTAs' shared memory and
+// B = K split by keys (rank r loads keys 64*r .. 64*r+63 of each tile); each
+// CTA's tensor memory receives S for its own 128 rows.  PV reads P from both
+// CTAs' tensor memory and V split by columns (rank r loads columns
+// 64*r .. 64*r+63).  Each CTA loads only its half of every K/V tile, so the
+// pair reads each tile from L2 once for 512 query rows.  Two cooperating
+// CTAs in a cluster are the direction the B300 G5 page ("Flash Attention
+// CUDA Kernel optimisation: from 56 to 986 TFLOPS on B300") names at its end
+// (section "next steps"); the per-CTA softmax, correction, epilogue and
+// scheduling are those of the single-CTA kernel in fa_prefill.cuh (whose
+// helpers this file uses).
+//
+// Roles per CTA (16 warps): softmax 0-7 (stage = warp / 4), epilogue 8-11,
+// warp 12 allocates tensor memory for the pair and, in the leader only,
+// issues every MMA, warp 13 loads this CTA's operands (in the leader it also
+// claims items and publishes them to both CTAs).  Barriers the MMA waits on
+// live in the leader and count arrivals from both CTAs; the MMA's commits
+// arrive in both CTAs (multicast); the follower's loads signal the leader's
+// barriers.
+#pragma once
+#include "fa_prefill.cuh"
+
+namespace fa {
+
+constexpr int kPairRows = 512;       // query rows per pair item
+constexpr int kPairStageRows = 256;  // per stage, 128 in each CTA
+// Takers of each item, both CTAs: leader MMA + 8 softmax + 4 epilogue warps,
+// follower 8 softmax + 4 epilogue + producer warps.
+constexpr int kPairTakers = 26;
+
+struct PairLayout {
+  static constexpr int D = 128;
+  static constexpr int kQBytes = kBM * D * 2;   // one stage of this CTA's Q (32 KB)
+  static constexpr int kBox = 128 * 64 * 2;     // 128 rows x 64 columns
+  static constexpr int kKBox = 64 * 64 * 2;     // 64 keys x 64 columns
+  static constexpr int kHalfBytes = 16384;      // this CTA's half of a K or V tile
+  static constexpr int kSlots = 8;
+  static constexpr int kOutWarpBytes = 32 * D * 2;
+  static constexpr int kOutBox = 32 * 64 * 2;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffKV = kOffQ + kStages * kQBytes;
+  static constexpr int kOffOut = kOffKV + kSlots * kHalfBytes;
+  static constexpr int kOffMisc = kOffOut + 4 * kOutWarpBytes;
+  // mbarrier indices (L: used in the leader only; B: in both CTAs)
+  static constexpr int Q_FULL = 0;     // [2] L: both CTAs' Q_s landed
+  static constexpr int Q_EMPTY = 2;    // [2] B: the item's last QK_s is done
+  static constexpr int S_FULL = 4;     // [2] B: S_s ready
+  static constexpr int PV_READY = 6;   // [2] L: P_s stored in both CTAs (8 warps)
+  static constexpr int O_READY = 8;    // [2] B: PV_s done
+  static constexpr int ML_FULL = 10;   // [2] B: the item's 1/l published (local)
+  static constexpr int O_FREE = 12;    // [2] L: both CTAs' epilogues read O_s (8 warps)
+  static constexpr int DRAIN = 14;     // L
+  static constexpr int ITEM_FULL = 15;   // [kItemRing] B: item published
+  static constexpr int ITEM_EMPTY = 19;  // [kItemRing] L: every taker of both CTAs read it
+  static constexpr int KV_FULL = 23;             // [kSlots] L: both halves landed
+  static constexpr int KV_EMPTY = 23 + kSlots;   // [kSlots] B: the MMAs that read it are done
+  static constexpr int kNumBars = 23 + 2 * kSlots;
+  static constexpr int kOffBars = kOffMisc;
+  static constexpr int kOffInvL = kOffBars + ((kNumBars * 8 + 15) / 16) * 16;
+  static constexpr int kOffItems = kOffInvL + kStages * kBM * 4;
+  static constexpr int kOffTmemSlot = kOffItems + kItemRing * 4;
+  static constexpr int kOffAbort = kOffTmemSlot + 4;
+  static constexpr int kMiscBytes = kOffAbort + 4 - kOffMisc;
+  static constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;  // + align
+  static constexpr int kTmemCols = 512;
+  static constexpr int kTmemO = 256;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+struct PairItem {
+  int bh, row0, nT0, nT1;
+};
+
+// Key tiles a 256-row stage whose first query row is `row_first` needs.
+__device__ __forceinline__ int pair_stage_tiles(int row_first, int Sq, int Skv, int causal) {
+  const int n_all = (Skv + kBN - 1) / kBN;
+  if (!causal) return n_all;
+  const int last_key = row_first + kPairStageRows - 1 + (Skv - Sq);
+  if (last_key < 0) return 0;
+  return min(n_all, last_key / kBN + 1);
+}
+
+// Pair item idx: heaviest first under causal LPT.
+__device__ __forceinline__ PairItem get_pair_item(const PrefillParams& p, int idx) {
+  PairItem it;
+  int qtile;
+  if (p.causal && p.lpt) {
+    qtile = p.n_qtiles - 1 - idx / p.BH;
+    it.bh = idx % p.BH;
+  } else {
+    qtile = idx % p.n_qtiles;
+    it.bh = idx / p.n_qtiles;
+  }
+  it.row0 = qtile * kPairRows;
+  it.nT0 = pair_stage_tiles(it.row0, p.Sq, p.Skv, p.causal);
+  it.nT1 = pair_stage_tiles(it.row0 + kPairStageRows, p.Sq, p.Skv, p.causal);
+  return it;
+}
+
+// Waits on barriers that another CTA's release-arrive completes (acquire at
+// cluster scope); out-of-line slow path as in wait_slow.
+template <unsigned kSleepNs>
+__device__ __noinline__ bool pair_wait_slow(uint32_t bar, uint32_t parity,
+                                            volatile uint32_t* abort_flag, unsigned* status,
+                                            unsigned long long timeout) {
+  uint64_t t0 = 0;
+  for (uint32_t n = 1;; ++n) {
+    if constexpr (kSleepNs > 0) __nanosleep(kSleepNs);
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((n & 7u) == 0) {
+      if (*abort_flag) return false;
+      const uint64_t t = globaltimer_ns();
+      if (t0 == 0) {
+        t0 = t;
+      } else if (t - t0 > timeout) {
+        *abort_flag = 1u;
+        atomicExch(status, kStatusTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+template <unsigned kSleepNs>
+__device__ __forceinline__ bool pair_wait_warp(uint32_t bar, uint32_t parity, const Ctl& c) {
+  const bool ok = mbar_try_wait_cluster(bar, parity) ||
+                  pair_wait_slow<kSleepNs>(bar, parity, c.abort, c.status, c.timeout);
+  return __all_sync(0xffffffffu, ok);
+}
+
+template <unsigned kSleepNs>
+__device__ __forceinline__ bool pair_wait_one(uint32_t bar, uint32_t parity, const Ctl& c) {
+  return mbar_try_wait_cluster(bar, parity) ||
+         pair_wait_slow<kSleepNs>(bar, parity, c.abort, c.status, c.timeout);
+}
+
+// The k-th item of this CTA from its ring (-1: no more); the arrival that
+// frees the ring slot goes to the leader's ITEM_EMPTY.
+template <unsigned kSleepNs>
+__device__ __forceinline__ int pair_take_item(const volatile int* ring, uint32_t full,
+                                              uint32_t empty_leader_cl, uint32_t k,
+                                              const Ctl& c, bool& ok) {
+  const uint32_t slot = k % kItemRing;
+  ok = pair_wait_warp<kSleepNs>(full + 8u * slot, (k / kItemRing) & 1, c);
+  const int idx = ok ? ring[slot] : -1;
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive_cluster(empty_leader_cl + 8u * slot);
+  return idx;
+}
+
+// Distinct sleep values from the single-CTA kernel's, so that no out-of-line
+// wait is shared between register regions of different sizes.
+constexpr unsigned kPairSleepSoftmaxNs = 1;
+constexpr unsigned kPairSleepMmaNs = 33;
+constexpr unsigned kPairSleepProducerNs = 65;
+constexpr unsigned kPairSleepEpilogueNs = 257;
+
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ,
+                           const __grid_constant__ CUtensorMap tmK,  // box: 64 keys
+                           const __grid_constant__ CUtensorMap tmV,
+                           const __grid_constant__ CUtensorMap tmO,
+                           const PrefillParams p) {
+  using L = PairLayout;
+  constexpr int D = L::D;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sQ = sbase + L::kOffQ;
+  const uint32_t sKV = sbase + L::kOffKV;
+  const uint32_t sOut = sbase + L::kOffOut;
+  const uint32_t bars = sbase + L::kOffBars;
+  float* inv_l_smem = reinterpret_cast<float*>(smem + L::kOffInvL);
+  volatile int* item_ring = reinterpret_cast<volatile int*>(smem + L::kOffItems);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffTmemSlot);
+  volatile uint32_t* abort_flag =
+      reinterpret_cast<volatile uint32_t*>(smem + L::kOffAbort);
+  auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  // the leader's barriers, as shared::cluster addresses (valid in both CTAs)
+  const uint32_t bars_l = mapa_shared(bars, 0);
+  auto bar_l = [&](int i) { return bars_l + 8u * static_cast<uint32_t>(i); };
+
+  // ---- setup ----
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(L::Q_FULL + s), 1);
+      mbar_init(bar(L::Q_EMPTY + s), 1);
+      mbar_init(bar(L::S_FULL + s), 1);
+      mbar_init(bar(L::PV_READY + s), 8);  // 4 softmax warps of the stage in each CTA
+      mbar_init(bar(L::O_READY + s), 1);
+      mbar_init(bar(L::ML_FULL + s), 4);
+      mbar_init(bar(L::O_FREE + s), 8);    // 4 epilogue warps in each CTA
+    }
+    mbar_init(bar(L::DRAIN), 1);
+    for (int i = 0; i < kItemRing; ++i) {
+      mbar_init(bar(L::ITEM_FULL + i), 1);
+      mbar_init(bar(L::ITEM_EMPTY + i), kPairTakers);
+    }
+    for (int i = 0; i < L::kSlots; ++i) {
+      mbar_init(bar(L::KV_FULL + i), 1);
+      mbar_init(bar(L::KV_EMPTY + i), 1);
+    }
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 12) {
+    tmem_alloc_pair(smem_u32(tmem_slot), L::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  if (warp == 13 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmO);
+  }
+  // both CTAs' barriers are initialised before either CTA signals the other's
+  tc_fence_before();
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Ctl ctl{abort_flag, p.status, p.timeout_ns};
+
+  const int wg = warp >> 2;
+  if (wg < 2) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+  } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
+  }
+
+  if (wg < 2) {
+    // ===================== softmax, stage s, this CTA's rows =====================
+    const int s = wg;
+    const int rq = warp & 3;
+    const int r = rq * 32 + lane;
+    const int off = p.Skv - p.Sq;
+    const uint32_t t_lane = static_cast<uint32_t>(rq * 32) << 16;
+    const uint32_t tS = tmem + t_lane + static_cast<uint32_t>(s * kBN);
+    const uint32_t tO = tmem + t_lane + static_cast<uint32_t>(L::kTmemO + s * D);
+    const float c = p.scale_log2;
+    const float tau = p.rescale_tau;
+    uint32_t n_s = 0;
+    bool ok = true;
+
+#pragma unroll 1
+    for (uint32_t k = 0; ok; ++k) {
+      const int idx = pair_take_item<kPairSleepSoftmaxNs>(item_ring, bar(L::ITEM_FULL),
+                                                          bar_l(L::ITEM_EMPTY), k, ctl, ok);
+      if (!ok || idx < 0) break;
+      const PairItem it = get_pair_item(p, idx);
+      const int nT = s == 0 ? it.nT0 : it.nT1;
+      const int stage_row0 = it.row0 + s * kPairStageRows + static_cast<int>(rank) * kBM;
+      const int row_g = stage_row0 + r;
+      float m = -INFINITY;
+      float l = 0.f;
+
+#pragma unroll 1
+      for (int j = 0; j < nT; ++j, ++n_s) {
+        if (!wait_bar_warp(bar(L::S_FULL + s), n_s & 1, ctl)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t sr[8][16];
+#pragma unroll
+        for (int cc = 0; cc < 8; cc += 2) tmem_ld32(tS + cc * 16, sr[cc], sr[cc + 1]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) reg_fence16(sr[cc]);
+
+        // mask: ragged key tail, and the causal diagonal (this CTA's rows;
+        // the pair's stage may reach one tile further than these rows need)
+        const int key0 = j * kBN;
+        const bool need_mask =
+            (key0 + kBN > p.Skv) || (p.causal && key0 + kBN - 1 > stage_row0 + off);
+        if (need_mask) {
+          int lim = p.Skv - 1 - key0;
+          if (p.causal) lim = min(lim, row_g + off - key0);
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc)
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              if (cc * 16 + e > lim) sr[cc][e] = __float_as_uint(-INFINITY);
+        }
+        float mx[16];
+#pragma unroll
+        for (int g = 0; g < 16; ++g) {
+          const uint32_t* v = &sr[g >> 1][(g & 1) * 8];
+          float a = fmax3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
+          a = fmax3(a, __uint_as_float(v[3]), __uint_as_float(v[4]));
+          a = fmax3(a, __uint_as_float(v[5]), __uint_as_float(v[6]));
+          mx[g] = fmaxf(a, __uint_as_float(v[7]));
+        }
+        const float r0 = fmax3(mx[0], mx[1], mx[2]), r1 = fmax3(mx[3], mx[4], mx[5]);
+        const float r2 = fmax3(mx[6], mx[7], mx[8]), r3 = fmax3(mx[9], mx[10], mx[11]);
+        const float r4 = fmax3(mx[12], mx[13], mx[14]);
+        const float t_max = fmaxf(fmax3(r0, r1, r2), fmax3(r3, r4, mx[15])) * c;
+        const float m_new = t_max > m + tau ? t_max : m;
+        const float m_use = m_new == -INFINITY ? 0.f : m_new;
+        const float alpha = m_new == m ? 1.f : ex2_approx(m - m_use);
+        const float neg_m = -m_use;
+        float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const int col = h * 32 + q * 4;
+            uint32_t* v = &sr[col >> 4][col & 15];
+            float x0, x1, x2, x3;
+            ffma2(x0, x1, __uint_as_float(v[0]), __uint_as_float(v[1]), c, c, neg_m, neg_m);
+            ffma2(x2, x3, __uint_as_float(v[2]), __uint_as_float(v[3]), c, c, neg_m, neg_m);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+            fadd2(l0, l1, l0, l1, p0, p1);
+            fadd2(l2, l3, l2, l3, p2, p3);
+            pk[2 * q] = pack2<BF16>(p0, p1);
+            pk[2 * q + 1] = pack2<BF16>(p2, p3);
+          }
+          tmem_st16(tS + h * 16, pk);
+        }
+        l = l * alpha + ((l0 + l1) + (l2 + l3));
+        m = m_new;
+        // O_s *= alpha (rare); PV_s(j-1) has completed: S_FULL_s(j) was
+        // committed after it
+        if (j > 0 && (p.always_rescale || __any_sync(0xffffffffu, alpha != 1.f))) {
+#pragma unroll 1
+          for (int cc = 0; cc < D / 16; ++cc) {
+            uint32_t v[16];
+            tmem_ld16(tO + cc * 16, v);
+            tmem_wait_ld();
+            reg_fence16(v);
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+            tmem_st16(tO + cc * 16, v);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster_relaxed(bar_l(L::PV_READY + s));
+      }
+      if (!ok) break;
+
+      if (row_g < p.Sq) {
+        const float lse = l > 0.f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+        p.lse[static_cast<size_t>(it.bh) * p.Sq + row_g] = lse;
+      }
+      if (nT > 0) {
+        if (!wait_bar_warp(bar(L::O_READY + s), (n_s - 1) & 1, ctl)) { ok = false; break; }
+        inv_l_smem[s * kBM + r] = l > 0.f ? 1.f / l : 0.f;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(L::ML_FULL + s));
+      }
+    }
+    __syncwarp();
+  } else if (wg == 2) {
+    // ========================= epilogue, this CTA's rows =========================
+    const int rq = warp & 3;
+    const int r = rq * 32 + lane;
+    const uint32_t t_lane = static_cast<uint32_t>(rq * 32) << 16;
+    const uint32_t stage_buf = sOut + static_cast<uint32_t>(rq * L::kOutWarpBytes);
+    uint32_t n_t0 = 0, n_t1 = 0;
+    uint32_t n_e0 = 0, n_e1 = 0;
+    bool ok = true;
+#pragma unroll 1
+    for (uint32_t k = 0; ok; ++k) {
+      const int idx = pair_take_item<kPairSleepEpilogueNs>(item_ring, bar(L::ITEM_FULL),
+                                                           bar_l(L::ITEM_EMPTY), k, ctl, ok);
+      if (!ok || idx < 0) break;
+      const PairItem it = get_pair_item(p, idx);
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        if (!ok) continue;
+        const int nT = s == 0 ? it.nT0 : it.nT1;
+        const bool have_o = nT > 0;
+        float inv_l = 0.f;
+        if (have_o) {
+          uint32_t& n_t = s == 0 ? n_t0 : n_t1;
+          uint32_t& n_e = s == 0 ? n_e0 : n_e1;
+          n_t += static_cast<uint32_t>(nT);
+          if (!wait_bar_warp<kSleepEpilogueNs>(bar(L::ML_FULL + s), n_e & 1, ctl)) { ok = false; continue; }
+          ++n_e;
+          inv_l = inv_l_smem[s * kBM + r];
+          if (!wait_bar_warp<kSleepEpilogueNs>(bar(L::O_READY + s), (n_t - 1) & 1, ctl)) { ok = false; continue; }
+          tc_fence_after();
+        }
+        const uint32_t tO = tmem + t_lane + static_cast<uint32_t>(L::kTmemO + s * D);
+        if (lane == 0) bulk_wait_group_read0();
+        __syncwarp();
+#pragma unroll 1
+        for (int cc = 0; cc < D / 16; ++cc) {
+          uint32_t v[16];
+          if (have_o) {
+            tmem_ld16(tO + cc * 16, v);
+            tmem_wait_ld();
+            reg_fence16(v);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = 0u;
+          }
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int col = cc * 16 + h * 8;
+            const uint32_t w0 = pack2<BF16>(__uint_as_float(v[h * 8 + 0]) * inv_l, __uint_as_float(v[h * 8 + 1]) * inv_l);
+            const uint32_t w1 = pack2<BF16>(__uint_as_float(v[h * 8 + 2]) * inv_l, __uint_as_float(v[h * 8 + 3]) * inv_l);
+            const uint32_t w2 = pack2<BF16>(__uint_as_float(v[h * 8 + 4]) * inv_l, __uint_as_float(v[h * 8 + 5]) * inv_l);
+            const uint32_t w3 = pack2<BF16>(__uint_as_float(v[h * 8 + 6]) * inv_l, __uint_as_float(v[h * 8 + 7]) * inv_l);
+            const int box = col >> 6, chunk = (col & 63) >> 3;
+            st_shared_v4(stage_buf + static_cast<uint32_t>(box * L::kOutBox + lane * 128 +
+                                                           ((chunk ^ (lane & 7)) << 4)),
+                         w0, w1, w2, w3);
+          }
+        }
+        if (have_o) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster_relaxed(bar_l(L::O_FREE + s));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        const int warp_row0 = it.row0 + s * kPairStageRows + static_cast<int>(rank) * kBM + rq * 32;
+        if (lane == 0 && warp_row0 < p.Sq) {
+#pragma unroll
+          for (int box = 0; box < D / 64; ++box)
+            tma_store_3d(&tmO, stage_buf + static_cast<uint32_t>(box * L::kOutBox), box * 64,
+                         warp_row0, it.bh);
+          bulk_commit_group();
+        }
+      }
+    }
+    if (lane == 0) bulk_wait_group0();
+    __syncwarp();
+  } else if (warp == 12 && leader) {
+    // ======================= MMA issuer (leader CTA only) =======================
+    // The single-CTA kernel's issue order, with pair MMAs: per item
+    // QK_0(0) QK_1(0), then per key tile PV_0(j) QK_0(j+1) PV_1(j) QK_1(j+1).
+    // Commits arrive in both CTAs.
+    {
+      constexpr uint16_t kBoth = 3;
+      constexpr uint32_t kIdescQK = idesc_f16(BF16, false, false, 2 * kBM, kBN);
+      constexpr uint32_t kIdescPV = idesc_f16(BF16, false, true, 2 * kBM, D);
+      const uint32_t tS0 = tmem, tS1 = tmem + kBN;
+      const uint32_t tO0 = tmem + L::kTmemO, tO1 = tmem + L::kTmemO + D;
+      bool issued = false;
+
+      auto slot_of = [&](int fill) { return fill % L::kSlots; };
+      auto par_of = [&](int fill) { return static_cast<uint32_t>((fill / L::kSlots) & 1); };
+      // QK_s: A = Q_s (2 boxes of 128 rows, +1024 descriptor units apart),
+      // B = this CTA's 64 keys of K (2 boxes of 64 rows, +512 units apart)
+      auto qk = [&](int s, int fk, bool last_of_stage) {
+        const uint64_t da = smem_desc_sw128(sQ + static_cast<uint32_t>(s * L::kQBytes), 16, 1024);
+        const uint64_t db = smem_desc_sw128(sKV + static_cast<uint32_t>(slot_of(fk) * L::kHalfBytes), 16, 1024);
+        umma_pair_ss_k128<L::kBox / 16, L::kKBox / 16>(s == 0 ? tS0 : tS1, da, db, kIdescQK, 0u);
+        umma_commit_pair(bar(L::S_FULL + s), kBoth);
+        if (last_of_stage) umma_commit_pair(bar(L::Q_EMPTY + s), kBoth);
+      };
+      // PV_s: A = P_s from both CTAs' tensor memory, B = this CTA's 64
+      // columns of V (one MN-major box)
+      auto pv = [&](int s, int fv, bool acc) {
+        umma_pair_ts_k128(s == 0 ? tO0 : tO1, s == 0 ? tS0 : tS1,
+                          smem_desc_sw128(sKV + static_cast<uint32_t>(slot_of(fv) * L::kHalfBytes),
+                                          L::kBox, 1024),
+                          kIdescPV, acc ? 1u : 0u);
+        umma_commit_pair(bar(L::O_READY + s), kBoth);
+      };
+      auto begin = [&](const PairItem& it, int kq, int f) -> bool {
+        if (!wait_bar_warp<kSleepMmaNs>(bar(L::Q_FULL + 0), kq & 1, ctl) ||
+            !wait_bar_warp<kSleepMmaNs>(bar(L::Q_FULL + 1), kq & 1, ctl))
+          return false;
+        if (it.nT1 > 0 && !wait_bar_warp<kSleepMmaNs>(bar(L::KV_FULL + slot_of(f)), par_of(f), ctl)) return false;
+        tc_fence_after();
+        if (it.nT0 > 0) qk(0, f, it.nT0 == 1); else umma_commit_pair(bar(L::Q_EMPTY + 0), kBoth);
+        if (it.nT1 > 0) {
+          qk(1, f, it.nT1 == 1);
+          umma_commit_pair(bar(L::KV_EMPTY + slot_of(f)), kBoth);
+        } else {
+          umma_commit_pair(bar(L::Q_EMPTY + 1), kBoth);
+        }
+        issued = true;
+        return true;
+      };
+
+      uint32_t n_pv0 = 0, n_pv1 = 0;
+      uint32_t n_o0 = 0, n_o1 = 0;
+      int kq = 0;
+      int fK = 0;
+      bool ok = true;
+      const int first = pair_take_item<kPairSleepMmaNs>(item_ring, bar(L::ITEM_FULL),
+                                                        bar_l(L::ITEM_EMPTY), 0, ctl, ok);
+      PairItem cur = first >= 0 ? get_pair_item(p, first) : PairItem{0, 0, 0, 0};
+      if (ok && first >= 0) ok = begin(cur, 0, 0);
+      else ok = false;
+#pragma unroll 1
+      while (ok) {
+        bool taken = false, has_next = false;
+        PairItem nxt{0, 0, 0, 0};
+        auto take_next = [&]() {
+          if (taken) return;
+          taken = true;
+          const int nidx = pair_take_item<kPairSleepMmaNs>(item_ring, bar(L::ITEM_FULL),
+                                                           bar_l(L::ITEM_EMPTY), kq + 1, ctl, ok);
+          has_next = ok && nidx >= 0;
+          if (has_next) nxt = get_pair_item(p, nidx);
+        };
+        const int fN = fK + 2 * cur.nT1;
+#pragma unroll 1
+        for (int j = 0; j < cur.nT1; ++j) {
+          const bool last = j + 1 == cur.nT1;
+          if (last) {
+            take_next();
+            if (!ok) break;
+          }
+          const int fv = fK + 2 * j + 1, fk1 = fK + 2 * j + 2;
+          bool rdy = mbar_try_wait(bar(L::KV_FULL + slot_of(fv)), par_of(fv));
+          if (j < cur.nT0) rdy &= mbar_try_wait_cluster(bar(L::PV_READY + 0), n_pv0 & 1);
+          if (!__all_sync(0xffffffffu, rdy)) {
+            if (!wait_bar_warp<kSleepMmaNs>(bar(L::KV_FULL + slot_of(fv)), par_of(fv), ctl)) { ok = false; break; }
+            if (j < cur.nT0 && !pair_wait_warp<kPairSleepMmaNs>(bar(L::PV_READY + 0), n_pv0 & 1, ctl)) { ok = false; break; }
+          }
+          if (j < cur.nT0) {
+            if (j == 0 && n_o0 > 0 && !pair_wait_warp<kPairSleepMmaNs>(bar(L::O_FREE + 0), (n_o0 - 1) & 1, ctl)) {
+              ok = false;
+              break;
+            }
+            ++n_pv0;
+            tc_fence_after();
+            pv(0, fv, j > 0);
+          }
+          if (!last && !wait_bar_warp<kSleepMmaNs>(bar(L::KV_FULL + slot_of(fk1)), par_of(fk1), ctl)) {
+            ok = false;
+            break;
+          }
+          if (!last) {
+            if (j + 1 < cur.nT0) qk(0, fk1, j + 2 == cur.nT0);
+          } else if (has_next) {
+            if (!wait_bar_warp<kSleepMmaNs>(bar(L::Q_FULL + 0), (kq + 1) & 1, ctl)) { ok = false; break; }
+            if (nxt.nT1 > 0 && !wait_bar_warp<kSleepMmaNs>(bar(L::KV_FULL + slot_of(fN)), par_of(fN), ctl)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            if (nxt.nT0 > 0) qk(0, fN, nxt.nT0 == 1); else umma_commit_pair(bar(L::Q_EMPTY + 0), kBoth);
+          }
+          if (!pair_wait_warp<kPairSleepMmaNs>(bar(L::PV_READY + 1), n_pv1 & 1, ctl)) { ok = false; break; }
+          if (j == 0 && n_o1 > 0 && !pair_wait_warp<kPairSleepMmaNs>(bar(L::O_FREE + 1), (n_o1 - 1) & 1, ctl)) {
+            ok = false;
+            break;
+          }
+          ++n_pv1;
+          tc_fence_after();
+          pv(1, fv, j > 0);
+          umma_commit_pair(bar(L::KV_EMPTY + slot_of(fv)), kBoth);
+          if (!last) {
+            qk(1, fk1, j + 2 == cur.nT1);
+            umma_commit_pair(bar(L::KV_EMPTY + slot_of(fk1)), kBoth);
+          } else if (has_next) {
+            if (!wait_bar_warp<kSleepMmaNs>(bar(L::Q_FULL + 1), (kq + 1) & 1, ctl)) { ok = false; break; }
+            tc_fence_after();
+            if (nxt.nT1 > 0) {
+              qk(1, fN, nxt.nT1 == 1);
+              umma_commit_pair(bar(L::KV_EMPTY + slot_of(fN)), kBoth);
+            } else {
+              umma_commit_pair(bar(L::Q_EMPTY + 1), kBoth);
+            }
+          }
+        }
+        if (ok) take_next();  // an item without key tiles
+        if (!ok || !has_next) break;
+        if (cur.nT0 > 0) ++n_o0;
+        if (cur.nT1 > 0) ++n_o1;
+        if (cur.nT1 == 0) ok = begin(nxt, kq + 1, fN);
+        ++kq;
+        cur = nxt;
+        fK = fN;
+      }
+      if (issued) {  // every MMA issued so far completes before TMEM is freed
+        umma_commit_pair(bar(L::DRAIN), 1);
+        wait_drain(bar(L::DRAIN), 0, p.timeout_ns);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 13) {
+    // ============================== TMA producers ==============================
+    // Both CTAs: per item Q_0, K_0, Q_1, V_0, then K_j V_j -- this CTA's rows
+    // of Q and its half of each K/V tile, completion on the leader's
+    // barriers (the leader expects both CTAs' bytes).  The leader also claims
+    // the items and publishes them to both CTAs.
+    if (lane == 0) {
+      int fill = 0;
+      int last_fill[L::kSlots];
+#pragma unroll
+      for (int i = 0; i < L::kSlots; ++i) last_fill[i] = -1;
+      int nq[2] = {0, 0};
+      bool ok = true;
+      const int qrow_off = static_cast<int>(rank) * kBM;
+      auto load_q = [&](const PairItem& it, int s) -> bool {
+        if (nq[s] > 0 && !wait_bar<kSleepProducerNs>(bar(L::Q_EMPTY + s), (nq[s] - 1) & 1, ctl)) return false;
+        if (leader) mbar_arrive_expect_tx(bar(L::Q_FULL + s), 2 * L::kQBytes);
+#pragma unroll
+        for (int box = 0; box < D / 64; ++box)
+          tma_load_3d_pair(sQ + static_cast<uint32_t>(s * L::kQBytes + box * L::kBox), &tmQ,
+                           bar_l(L::Q_FULL + s), box * 64,
+                           it.row0 + s * kPairStageRows + qrow_off, it.bh);
+        ++nq[s];
+        return true;
+      };
+      auto load_kv = [&](const PairItem& it, int kv, int j) -> bool {
+        const int slot = fill % L::kSlots;
+        const uint32_t par = static_cast<uint32_t>(((fill / L::kSlots) & 1) ^ 1);
+        if (!wait_bar<kSleepProducerNs>(bar(L::KV_EMPTY + slot), par, ctl)) return false;
+        if (p.test_stall && fill == 2) {  // test hook: both CTAs withhold the first K_1
+          ++fill;
+          return true;
+        }
+        if (leader) mbar_arrive_expect_tx(bar(L::KV_FULL + slot), 2 * L::kHalfBytes);
+        const uint32_t dst = sKV + static_cast<uint32_t>(slot * L::kHalfBytes);
+        if (kv == 0) {  // keys 64*rank .. of tile j, both 64-column boxes
+#pragma unroll
+          for (int box = 0; box < D / 64; ++box)
+            tma_load_3d_pair(dst + static_cast<uint32_t>(box * L::kKBox), &tmK,
+                             bar_l(L::KV_FULL + slot), box * 64,
+                             j * kBN + static_cast<int>(rank) * 64, it.bh);
+        } else {        // columns 64*rank .. of tile j, all 128 keys
+          tma_load_3d_pair(dst, &tmV, bar_l(L::KV_FULL + slot), static_cast<int>(rank) * 64,
+                           j * kBN, it.bh);
+        }
+        last_fill[slot] = fill;
+        ++fill;
+        return true;
+      };
+      const uint32_t ring_f = mapa_shared(smem_u32(const_cast<int*>(item_ring)), 1);
+      const uint32_t bars_f = mapa_shared(bars, 1);
+      int idx = static_cast<int>(blockIdx.x >> 1);  // the grid never exceeds 2x the items
+#pragma unroll 1
+      for (uint32_t k = 0; ok; ++k) {
+        const uint32_t slot = k % kItemRing;
+        if (leader) {
+          // publish item k (or the end) to both CTAs once every taker of
+          // both has taken item k - 4
+          const uint32_t par = (k / kItemRing - 1) & 1;
+          if (k >= kItemRing && !mbar_try_wait_cluster(bar(L::ITEM_EMPTY + slot), par) &&
+              !pair_wait_slow<kPairSleepProducerNs>(bar(L::ITEM_EMPTY + slot), par, ctl.abort,
+                                                    ctl.status, ctl.timeout)) {
+            ok = false;
+            break;
+          }
+          item_ring[slot] = idx;
+          st_shared_cluster_u32(ring_f + 4u * slot, static_cast<uint32_t>(idx));
+          mbar_arrive(bar(L::ITEM_FULL + slot));
+          mbar_arrive_cluster(bars_f + 8u * static_cast<uint32_t>(L::ITEM_FULL + slot));
+        } else {
+          if (!mbar_try_wait_cluster(bar(L::ITEM_FULL + slot), (k / kItemRing) & 1) &&
+              !pair_wait_slow<kPairSleepProducerNs>(bar(L::ITEM_FULL + slot), (k / kItemRing) & 1,
+                                                    ctl.abort, ctl.status, ctl.timeout)) {
+            ok = false;
+            break;
+          }
+          idx = item_ring[slot];
+          mbar_arrive_cluster(bar_l(L::ITEM_EMPTY + slot));
+        }
+        if (idx < 0) break;
+        const PairItem it = get_pair_item(p, idx);
+        ok = load_q(it, 0);
+#pragma unroll 1
+        for (int j = 0; ok && j < it.nT1; ++j) {
+          ok = load_kv(it, 0, j);
+          if (ok && j == 0) ok = load_q(it, 1);
+          if (ok) ok = load_kv(it, 1, j);
+        }
+        if (ok && it.nT1 == 0) ok = load_q(it, 1);
+        if (leader) {
+          const unsigned long long ticket = atomicAdd(p.sched, 1ull);
+          const unsigned long long nidx = (gridDim.x >> 1) + ticket;
+          idx = nidx < static_cast<unsigned long long>(p.n_items) ? static_cast<int>(nidx) : -1;
+        }
+      }
+      // drain (leader): its barriers complete only when both CTAs' loads
+      // have landed; the follower exits after the final cluster barrier
+      if (leader) {
+#pragma unroll
+        for (int s = 0; s < 2; ++s)
+          if (nq[s] > 0) wait_drain(bar(L::Q_FULL + s), (nq[s] - 1) & 1, p.timeout_ns);
+#pragma unroll 1
+        for (int i = 0; i < L::kSlots; ++i)
+          if (last_fill[i] >= 0)
+            wait_drain(bar(L::KV_FULL + i), static_cast<uint32_t>((last_fill[i] / L::kSlots) & 1),
+                       p.timeout_ns);
+      }
+    }
+    __syncwarp();
+  }
+
+  // ---- teardown: both CTAs finish before either frees tensor memory or
+  // exits (the leader's MMAs and the follower's loads touch both) ----
+  tc_fence_before();
+  cluster_sync_all();
+  if (warp == 12) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, L::kTmemCols);
+  }
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(&p.sched[1], 1ull) == gridDim.x - 1) {
+      p.sched[0] = 0ull;
+      p.sched[1] = 0ull;
+      __threadfence();
+    }
+  }
+}
+
+}  // namespace fa

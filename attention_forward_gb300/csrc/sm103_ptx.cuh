@@ -313,6 +313,191 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
       : "memory");
 }
 
+// ------------------------------------------------------------ CTA pairs
+// (a cluster of two CTAs whose tensor cores act as one: tcgen05 with
+// .cta_group::2, M = 256 with 128 rows in each CTA)
+
+// Rank of this CTA in its cluster.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// The shared::cluster address of the variable at shared address `a` of this
+// CTA, in the CTA of cluster rank `rank` (the same offset there).
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t a, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  return r;
+}
+
+// Arrive on an mbarrier of any CTA of the cluster (release, cluster scope).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cl_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cl_addr)
+               : "memory");
+}
+
+// Arrive on an mbarrier of any CTA of the cluster with relaxed semantics: no
+// release fence (a release arrive at cluster scope measured ~1500 cycles).
+// For arrivals that publish only tensor-memory accesses the arriving thread
+// has already waited for (tcgen05.wait::st / wait::ld, then
+// tcgen05.fence::before_thread_sync); the waiter follows its wait with
+// tcgen05.fence::after_thread_sync.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cl_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cl_addr)
+               : "memory");
+}
+
+// As mbar_try_wait, with acquire at cluster scope (for phases completed by
+// another CTA's release-arrive).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// As mbar_try_wait_cluster, without suspending the thread.
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// 32-bit store to the shared memory of another CTA of the cluster.
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cl_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cl_addr), "r"(v) : "memory");
+}
+
+// Every thread of both CTAs (release / acquire at cluster scope).
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::
+          : "memory");
+}
+
+// 3-D tiled load into this CTA's shared memory whose completion is signalled
+// on `bar_cl`, an mbarrier of either CTA of the pair (shared::cluster address).
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void* desc,
+                                                 uint32_t bar_cl, int32_t x, int32_t y,
+                                                 int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::"
+      "complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(desc)), "r"(bar_cl), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+// TMEM allocation for a CTA pair: one warp of each CTA executes it.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst, uint32_t ncols) {
+  asm volatile(
+      "tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst),
+      "r"(ncols)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr),
+               "r"(ncols)
+               : "memory");
+}
+
+// Eight K=16 steps of a pair MMA, D (+)= A * B, both operands K-major and
+// 128-byte swizzled in shared memory (the same offsets in both CTAs; A: this
+// CTA's 128 rows, B: this CTA's half of N).  The second 64-column box of A
+// starts `a_box` descriptor units (16 bytes) after the first, B's `b_box`.
+// Issued by the leader CTA's warp (elect.sync inside).
+template <int kABox, int kBBox>
+__device__ __forceinline__ void umma_pair_ss_k128(uint32_t d_tmem, uint64_t a_desc,
+                                                  uint64_t b_desc, uint32_t idesc,
+                                                  uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e, t;\n\t"
+      ".reg .b64 a1, a2, a3, a4, a5, a6, a7, b1, b2, b3, b4, b5, b6, b7;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 t, 0, 0;\n\t"
+      "add.s64 a1, %1, 2;\n\t add.s64 b1, %2, 2;\n\t"
+      "add.s64 a2, %1, 4;\n\t add.s64 b2, %2, 4;\n\t"
+      "add.s64 a3, %1, 6;\n\t add.s64 b3, %2, 6;\n\t"
+      "add.s64 a4, %1, %5;\n\t add.s64 b4, %2, %6;\n\t"
+      "add.s64 a5, a4, 2;\n\t add.s64 b5, b4, 2;\n\t"
+      "add.s64 a6, a4, 4;\n\t add.s64 b6, b4, 4;\n\t"
+      "add.s64 a7, a4, 6;\n\t add.s64 b7, b4, 6;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a1, b1, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a2, b2, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a3, b3, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a4, b4, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a5, b5, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a6, b6, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a7, b7, %3, t;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "n"(kABox), "n"(kBBox)
+      : "memory");
+}
+
+// Eight K=16 steps of a pair MMA with A in tensor memory (each CTA's 128
+// rows, 8 columns per step) and B MN-major 128-byte swizzled in shared
+// memory, 16 K rows (128 descriptor units) per step.
+__device__ __forceinline__ void umma_pair_ts_k128(uint32_t d_tmem, uint32_t a_tmem,
+                                                  uint64_t b_desc, uint32_t idesc,
+                                                  uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e, t;\n\t"
+      ".reg .b32 a1, a2, a3, a4, a5, a6, a7;\n\t"
+      ".reg .b64 b1, b2, b3, b4, b5, b6, b7;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 t, 0, 0;\n\t"
+      "add.s32 a1, %1, 8;\n\t  add.s64 b1, %2, 128;\n\t"
+      "add.s32 a2, %1, 16;\n\t add.s64 b2, %2, 256;\n\t"
+      "add.s32 a3, %1, 24;\n\t add.s64 b3, %2, 384;\n\t"
+      "add.s32 a4, %1, 32;\n\t add.s64 b4, %2, 512;\n\t"
+      "add.s32 a5, %1, 40;\n\t add.s64 b5, %2, 640;\n\t"
+      "add.s32 a6, %1, 48;\n\t add.s64 b6, %2, 768;\n\t"
+      "add.s32 a7, %1, 56;\n\t add.s64 b7, %2, 896;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [a1], b1, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [a2], b2, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [a3], b3, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [a4], b4, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [a5], b5, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [a6], b6, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [a7], b7, %3, t;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on the mbarrier at shared offset `bar` in each CTA of
+// `cta_mask` when every pair MMA issued so far by the elected lane has
+// completed.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster."
+      "multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }

@@ -22,6 +22,8 @@ FA_ERR_CUDA, FA_ERR_WORKSPACE, FA_ERR_TIMEOUT = 3, 4, 5
 FA_FLAG_NO_LPT = 0x1
 FA_FLAG_ALWAYS_RESCALE = 0x2
 FA_FLAG_EXACT_MAX = 0x4
+FA_FLAG_PAIR = 0x8
+FA_FLAG_SINGLE_CTA = 0x10
 FA_FLAG_TEST_STALL = 0x100
 
 _DTYPE = {torch.float16: FA_F16, torch.bfloat16: FA_BF16}
@@ -69,6 +71,8 @@ def load() -> ctypes.CDLL:
     L.fa_set_watchdog_ns.restype = None
     L.fa_status_string.argtypes = [ci]
     L.fa_status_string.restype = ctypes.c_char_p
+    L.fa_prefill_uses_pairs.argtypes = [ci, ci, ci, ci, ci, ci, ctypes.c_uint, ci]
+    L.fa_prefill_uses_pairs.restype = ci
     L.fa_version.argtypes = []
     L.fa_version.restype = ci
     _lib = L
@@ -210,6 +214,12 @@ def fa_set_watchdog_ns(ns: int) -> None:
 
 def fa_status_string(status: int) -> str:
     return load().fa_status_string(int(status)).decode()
+
+
+def fa_prefill_uses_pairs(B: int, H: int, Sq: int, Skv: int, D: int, causal: bool,
+                          flags: int = 0, num_splits: int = 0) -> bool:
+    return bool(load().fa_prefill_uses_pairs(B, H, Sq, Skv, D, int(bool(causal)), flags,
+                                              num_splits))
 
 
 def fa_version() -> int:

@@ -397,7 +397,9 @@ def bench_ours(args, w):
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": profiled_traffic("prefill", w.name),
                 "peak_source": f"{peak_src} bf16_tflops (burst; dense fp16 has the same rate)",
-                "kernel": "fa_prefill_kernel"}
+                "kernel": ("fa_prefill_pair_kernel (two-CTA clusters)"
+                           if fa.fa_prefill_uses_pairs(w.B, w.H, w.Sq, w.Skv, w.D, w.causal)
+                           else "fa_prefill_kernel")}
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,

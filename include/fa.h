@@ -74,6 +74,18 @@ typedef enum {
                                         more than 8 in log2 units; both are
                                         exact after the final division by
                                         the row sum                         */
+#define FA_FLAG_PAIR 0x8u            /* prefill, D = 128, without a key
+                                        split: run on CTA pairs (two-CTA
+                                        clusters whose tensor cores compute
+                                        256-row MMAs together, each CTA
+                                        loading half of every K/V tile);
+                                        ignored otherwise.  Without this flag
+                                        or FA_FLAG_SINGLE_CTA the library
+                                        uses pairs for long rows (non-causal
+                                        Sq, Skv >= 4096; causal Sq >= 16384)
+                                        with at least one 512-row item per
+                                        two SMs                             */
+#define FA_FLAG_SINGLE_CTA 0x10u     /* prefill: never use CTA pairs        */
 #define FA_FLAG_TEST_STALL 0x100u    /* test hook: the K/V producer of every
                                         CTA withholds its first item's second
                                         K tile, so the consumers' bounded
@@ -82,8 +94,10 @@ typedef enum {
 
 /*
  * fa_fwd -- the whole forward pass for one batch, on `stream`.
- * Prefill (Sq > 1): one fused, persistent kernel (one CTA per SM); its CTAs
- * claim work items from a counter in a small static device array of the
+ * Prefill (Sq > 1): one fused, persistent kernel (one CTA per SM, or one
+ * two-CTA cluster per pair of SMs for long rows at D = 128: see
+ * FA_FLAG_PAIR); its CTAs claim work items from a counter in a small static
+ * device array of the
  * library (1024 slots of 16 bytes, one per launch in turn, cleared by each
  * launch's last CTA), so two prefill launches whose GPU work overlaps must
  * be fewer than 1024 calls apart.  When the (256-row query tile, head)
@@ -191,6 +205,12 @@ void fa_set_watchdog_ns(unsigned long long ns);
 
 /* Static description of a status code (never NULL). */
 const char *fa_status_string(fa_status_t status);
+
+/* 1 if fa_fwd / fa_fwd_ex with these arguments runs prefill on CTA pairs
+ * (see FA_FLAG_PAIR), else 0 (single-CTA kernel, decode, or arguments fa_fwd
+ * would reject).  Reads the current device's SM count; launches nothing. */
+int fa_prefill_uses_pairs(int B, int H, int Sq, int Skv, int D, int causal,
+                          unsigned flags, int num_splits);
 
 /* Library ABI version: major * 10000 + minor * 100 + patch. */
 int fa_version(void);

@@ -29,7 +29,8 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("fa_fwd", "fa_fwd_ex", "fa_workspace_bytes", "fa_fwd_host",
               "fa_host_staging_bytes", "fa_get_device_status",
-              "fa_set_watchdog_ns", "fa_status_string", "fa_version"):
+              "fa_set_watchdog_ns", "fa_status_string", "fa_version",
+              "fa_prefill_uses_pairs"):
         assert n in names, n
 
 
@@ -43,7 +44,25 @@ def test_status_strings_and_version(lib):
     for st in range(6):
         assert fa.fa_status_string(st)
     assert fa.fa_status_string(99) == "unknown status"
-    assert fa.fa_version() == 10000
+    assert fa.fa_version() == 10100
+
+
+def test_pair_selection_without_a_gpu(lib):
+    """The CTA-pair choice on the host (no device: SM count unknown, the
+    default rule assumes 152 SMs): forced and refused by the flags, never for
+    D=64, decode or a key split, by default only for long rows."""
+    from attention_forward_gb300 import fa
+    P, S = fa.FA_FLAG_PAIR, fa.FA_FLAG_SINGLE_CTA
+    assert fa.fa_prefill_uses_pairs(1, 1, 300, 300, 128, True, P)
+    assert not fa.fa_prefill_uses_pairs(4, 16, 4096, 4096, 128, False, S)
+    assert not fa.fa_prefill_uses_pairs(1, 1, 300, 300, 64, True, P)
+    assert not fa.fa_prefill_uses_pairs(1, 1, 1, 300, 128, False, P)
+    assert not fa.fa_prefill_uses_pairs(1, 1, 300, 300, 128, False, P, num_splits=2)
+    assert fa.fa_prefill_uses_pairs(4, 16, 4096, 4096, 128, False)
+    assert not fa.fa_prefill_uses_pairs(4, 16, 2048, 2048, 128, False)
+    assert not fa.fa_prefill_uses_pairs(1, 16, 8192, 8192, 128, True)
+    assert fa.fa_prefill_uses_pairs(1, 16, 16384, 16384, 128, True)
+    assert not fa.fa_prefill_uses_pairs(1, 1, 4096, 4096, 128, False)  # 8 items
 
 
 def _call(lib, q=16, k=16, v=16, o=16, lse=16, B=1, H=1, Sq=8, Skv=8, D=64,
