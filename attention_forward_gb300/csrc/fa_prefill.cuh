@@ -281,6 +281,139 @@ __device__ __forceinline__ int take_item(const volatile int* ring, uint32_t full
   return idx;
 }
 
+// One key tile of one stage's softmax, for this thread's query row (its TMEM
+// lane): load S (128 fp32 columns at tS) into registers, mask keys past the
+// ragged end and past the causal diagonal (key0: the tile's first key;
+// stage_row0: the first of the 128 rows that share this TMEM quarter's tile;
+// row_g: this thread's row), raise the reference max m past the threshold,
+// write P = 2^(c*s - m) as packed 16-bit pairs over the first 64 columns of S,
+// update the row sum l, and rescale this warp's rows of O (D columns at tO)
+// when one of them moved its reference max.  Ends with tcgen05.wait::st.
+template <int D, bool BF16>
+__device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int key0, int stage_row0,
+                                             int row_g, const PrefillParams& p, bool may_rescale,
+                                             float& m, float& l) {
+  const int off = p.Skv - p.Sq;
+  const float c = p.scale_log2;
+  const float tau = p.rescale_tau;
+  uint32_t sr[8][16];
+#pragma unroll
+  for (int cc = 0; cc < 8; cc += 2) tmem_ld32(tS + cc * 16, sr[cc], sr[cc + 1]);
+  tmem_wait_ld();
+#pragma unroll
+  for (int cc = 0; cc < 8; ++cc) reg_fence16(sr[cc]);
+
+  // mask: ragged key tail, and the causal diagonal
+  const bool need_mask =
+      (key0 + kBN > p.Skv) || (p.causal && key0 + kBN - 1 > stage_row0 + off);
+  if (need_mask) {
+    int lim = p.Skv - 1 - key0;
+    if (p.causal) lim = min(lim, row_g + off - key0);
+#pragma unroll
+    for (int cc = 0; cc < 8; ++cc)
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        if (cc * 16 + e > lim) sr[cc][e] = __float_as_uint(-INFINITY);
+  }
+  // row max as a shallow tree: 16 independent 8-column maxima, then 3 levels
+  float mx[16];
+#pragma unroll
+  for (int g = 0; g < 16; ++g) {
+    const uint32_t* v = &sr[g >> 1][(g & 1) * 8];
+    float a = fmax3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
+    a = fmax3(a, __uint_as_float(v[3]), __uint_as_float(v[4]));
+    a = fmax3(a, __uint_as_float(v[5]), __uint_as_float(v[6]));
+    mx[g] = fmaxf(a, __uint_as_float(v[7]));
+  }
+  const float r0 = fmax3(mx[0], mx[1], mx[2]), r1 = fmax3(mx[3], mx[4], mx[5]);
+  const float r2 = fmax3(mx[6], mx[7], mx[8]), r3 = fmax3(mx[9], mx[10], mx[11]);
+  const float r4 = fmax3(mx[12], mx[13], mx[14]);
+  const float t_max = fmaxf(fmax3(r0, r1, r2), fmax3(r3, r4, mx[15])) * c;
+  // raise the reference max only past the threshold (m = -inf: always)
+  const float m_new = t_max > m + tau ? t_max : m;
+  const float m_use = m_new == -INFINITY ? 0.f : m_new;
+  const float alpha = m_new == m ? 1.f : ex2_approx(m - m_use);
+  const float neg_m = -m_use;
+  // p = 2^(s*c - m) in four 32-column pieces: the argument as packed
+  // fp32x2 FMAs, the row sum as packed fp32x2 adds; each piece is packed
+  // to 16-bit pairs and stored over the first 64 columns of S_s (every S
+  // value of this row is already in registers) while the next piece's
+  // exponentials run
+  float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int col = h * 32 + q * 4;
+      uint32_t* v = &sr[col >> 4][col & 15];
+      float x0, x1, x2, x3;
+      ffma2(x0, x1, __uint_as_float(v[0]), __uint_as_float(v[1]), c, c, neg_m, neg_m);
+      ffma2(x2, x3, __uint_as_float(v[2]), __uint_as_float(v[3]), c, c, neg_m, neg_m);
+      const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+      const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+      fadd2(l0, l1, l0, l1, p0, p1);
+      fadd2(l2, l3, l2, l3, p2, p3);
+      pk[2 * q] = pack2<BF16>(p0, p1);
+      pk[2 * q + 1] = pack2<BF16>(p2, p3);
+    }
+    tmem_st16(tS + h * 16, pk);
+  }
+  l = l * alpha + ((l0 + l1) + (l2 + l3));
+  m = m_new;
+  // O *= alpha when a row of this warp moved its reference max (rare: tau
+  // keeps it still).  The caller guarantees that the previous PV into O has
+  // completed (the kernels commit S_FULL after it) and passes may_rescale =
+  // false on an item's first tile, which has no O to rescale.
+  if (may_rescale && (p.always_rescale || __any_sync(0xffffffffu, alpha != 1.f))) {
+#pragma unroll 1
+    for (int cc = 0; cc < D / 16; ++cc) {
+      uint32_t v[16];
+      tmem_ld16(tO + cc * 16, v);
+      tmem_wait_ld();
+      reg_fence16(v);
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+      tmem_st16(tO + cc * 16, v);
+    }
+  }
+  tmem_wait_st();
+}
+
+// The epilogue's staging of 32 rows x D columns of O (this warp's TMEM lane
+// quarter at tO): O * inv_l rounded to 16 bits (zeros when the rows saw no
+// key), written to the warp's slice of shared memory as D/64 boxes of 32 rows
+// x 128 bytes, 128-byte swizzled, ready for the TMA store.
+template <int D, bool BF16>
+__device__ __forceinline__ void stage_o_rows(uint32_t tO, bool have_o, float inv_l,
+                                             uint32_t stage_buf, int out_box_bytes, int lane) {
+#pragma unroll 1
+  for (int cc = 0; cc < D / 16; ++cc) {
+    uint32_t v[16];
+    if (have_o) {
+      tmem_ld16(tO + cc * 16, v);
+      tmem_wait_ld();
+      reg_fence16(v);
+    } else {  // no visible key: O = 0
+#pragma unroll
+      for (int e = 0; e < 16; ++e) v[e] = 0u;
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int col = cc * 16 + h * 8;  // first column of this 16-byte chunk
+      const uint32_t w0 = pack2<BF16>(__uint_as_float(v[h * 8 + 0]) * inv_l, __uint_as_float(v[h * 8 + 1]) * inv_l);
+      const uint32_t w1 = pack2<BF16>(__uint_as_float(v[h * 8 + 2]) * inv_l, __uint_as_float(v[h * 8 + 3]) * inv_l);
+      const uint32_t w2 = pack2<BF16>(__uint_as_float(v[h * 8 + 4]) * inv_l, __uint_as_float(v[h * 8 + 5]) * inv_l);
+      const uint32_t w3 = pack2<BF16>(__uint_as_float(v[h * 8 + 6]) * inv_l, __uint_as_float(v[h * 8 + 7]) * inv_l);
+      const int box = col >> 6, chunk = (col & 63) >> 3;
+      st_shared_v4(stage_buf + static_cast<uint32_t>(box * out_box_bytes + lane * 128 +
+                                                     ((chunk ^ (lane & 7)) << 4)),
+                   w0, w1, w2, w3);
+    }
+  }
+}
+
 template <int D, bool BF16, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_prefill_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -358,12 +491,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int s = wg;
     const int rq = warp & 3;                 // lane quarter of TMEM
     const int r = rq * 32 + lane;            // row within the stage
-    const int off = p.Skv - p.Sq;
     const uint32_t t_lane = static_cast<uint32_t>(rq * 32) << 16;
     const uint32_t tS = tmem + t_lane + static_cast<uint32_t>(s * kBN);
     const uint32_t tO = tmem + t_lane + static_cast<uint32_t>(L::kTmemO + s * D);
-    const float c = p.scale_log2;
-    const float tau = p.rescale_tau;
     uint32_t n_s = 0;  // tiles of this stage so far (S_FULL / O_READY phase)
     bool ok = true;
 
@@ -382,89 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < nT; ++j, ++n_s) {
         if (!wait_bar_warp(bar(L::S_FULL + s), n_s & 1, ctl)) { ok = false; break; }
         tc_fence_after();
-        uint32_t sr[8][16];
-#pragma unroll
-        for (int cc = 0; cc < 8; cc += 2) tmem_ld32(tS + cc * 16, sr[cc], sr[cc + 1]);
-        tmem_wait_ld();
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) reg_fence16(sr[cc]);
-
-        // mask: ragged key tail, and the causal diagonal
-        const int key0 = (it.t0 + j) * kBN;
-        const bool need_mask =
-            (key0 + kBN > p.Skv) || (p.causal && key0 + kBN - 1 > stage_row0 + off);
-        if (need_mask) {
-          int lim = p.Skv - 1 - key0;
-          if (p.causal) lim = min(lim, row_g + off - key0);
-#pragma unroll
-          for (int cc = 0; cc < 8; ++cc)
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-              if (cc * 16 + e > lim) sr[cc][e] = __float_as_uint(-INFINITY);
-        }
-        // row max as a shallow tree: 16 independent 8-column maxima, then 3 levels
-        float mx[16];
-#pragma unroll
-        for (int g = 0; g < 16; ++g) {
-          const uint32_t* v = &sr[g >> 1][(g & 1) * 8];
-          float a = fmax3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
-          a = fmax3(a, __uint_as_float(v[3]), __uint_as_float(v[4]));
-          a = fmax3(a, __uint_as_float(v[5]), __uint_as_float(v[6]));
-          mx[g] = fmaxf(a, __uint_as_float(v[7]));
-        }
-        const float r0 = fmax3(mx[0], mx[1], mx[2]), r1 = fmax3(mx[3], mx[4], mx[5]);
-        const float r2 = fmax3(mx[6], mx[7], mx[8]), r3 = fmax3(mx[9], mx[10], mx[11]);
-        const float r4 = fmax3(mx[12], mx[13], mx[14]);
-        const float t_max = fmaxf(fmax3(r0, r1, r2), fmax3(r3, r4, mx[15])) * c;
-        // raise the reference max only past the threshold (m = -inf: always)
-        const float m_new = t_max > m + tau ? t_max : m;
-        const float m_use = m_new == -INFINITY ? 0.f : m_new;
-        const float alpha = m_new == m ? 1.f : ex2_approx(m - m_use);
-        const float neg_m = -m_use;
-        // p = 2^(s*c - m) in four 32-column pieces: the argument as packed
-        // fp32x2 FMAs, the row sum as packed fp32x2 adds; each piece is packed
-        // to 16-bit pairs and stored over the first 64 columns of S_s (every S
-        // value of this row is already in registers) while the next piece's
-        // exponentials run
-        float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const int col = h * 32 + q * 4;
-            uint32_t* v = &sr[col >> 4][col & 15];
-            float x0, x1, x2, x3;
-            ffma2(x0, x1, __uint_as_float(v[0]), __uint_as_float(v[1]), c, c, neg_m, neg_m);
-            ffma2(x2, x3, __uint_as_float(v[2]), __uint_as_float(v[3]), c, c, neg_m, neg_m);
-            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-            const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
-            fadd2(l0, l1, l0, l1, p0, p1);
-            fadd2(l2, l3, l2, l3, p2, p3);
-            pk[2 * q] = pack2<BF16>(p0, p1);
-            pk[2 * q + 1] = pack2<BF16>(p2, p3);
-          }
-          tmem_st16(tS + h * 16, pk);
-        }
-        l = l * alpha + ((l0 + l1) + (l2 + l3));
-        m = m_new;
-        // O_s *= alpha when a row of this warp moved its reference max (rare:
-        // tau keeps it still).  PV_s(j-1) has completed: S_FULL_s(j) was
-        // committed after it.  Tile 0 has no O of this item to rescale.
-        if (j > 0 && (p.always_rescale || __any_sync(0xffffffffu, alpha != 1.f))) {
-#pragma unroll 1
-          for (int cc = 0; cc < D / 16; ++cc) {
-            uint32_t v[16];
-            tmem_ld16(tO + cc * 16, v);
-            tmem_wait_ld();
-            reg_fence16(v);
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-              v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-            tmem_st16(tO + cc * 16, v);
-          }
-        }
-        tmem_wait_st();
+        softmax_tile<D, BF16>(tS, tO, (it.t0 + j) * kBN, stage_row0, row_g, p, j > 0, m, l);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(L::PV_READY + s));
@@ -560,30 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the slice is free once the previous store has read it
         if (lane == 0) bulk_wait_group_read0();
         __syncwarp();
-#pragma unroll 1
-        for (int cc = 0; cc < D / 16; ++cc) {
-          uint32_t v[16];
-          if (have_o) {
-            tmem_ld16(tO + cc * 16, v);
-            tmem_wait_ld();
-            reg_fence16(v);
-          } else {  // no visible key: O = 0
-#pragma unroll
-            for (int e = 0; e < 16; ++e) v[e] = 0u;
-          }
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int col = cc * 16 + h * 8;  // first column of this 16-byte chunk
-            const uint32_t w0 = pack2<BF16>(__uint_as_float(v[h * 8 + 0]) * inv_l, __uint_as_float(v[h * 8 + 1]) * inv_l);
-            const uint32_t w1 = pack2<BF16>(__uint_as_float(v[h * 8 + 2]) * inv_l, __uint_as_float(v[h * 8 + 3]) * inv_l);
-            const uint32_t w2 = pack2<BF16>(__uint_as_float(v[h * 8 + 4]) * inv_l, __uint_as_float(v[h * 8 + 5]) * inv_l);
-            const uint32_t w3 = pack2<BF16>(__uint_as_float(v[h * 8 + 6]) * inv_l, __uint_as_float(v[h * 8 + 7]) * inv_l);
-            const int box = col >> 6, chunk = (col & 63) >> 3;
-            st_shared_v4(stage_buf + static_cast<uint32_t>(box * L::kOutBox + lane * 128 +
-                                                           ((chunk ^ (lane & 7)) << 4)),
-                         w0, w1, w2, w3);
-          }
-        }
+        stage_o_rows<D, BF16>(tO, have_o, inv_l, stage_buf, L::kOutBox, lane);
         if (have_o) {
           tc_fence_before();
           __syncwarp();

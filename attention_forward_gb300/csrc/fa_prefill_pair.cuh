@@ -246,12 +246,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int s = wg;
     const int rq = warp & 3;
     const int r = rq * 32 + lane;
-    const int off = p.Skv - p.Sq;
     const uint32_t t_lane = static_cast<uint32_t>(rq * 32) << 16;
     const uint32_t tS = tmem + t_lane + static_cast<uint32_t>(s * kBN);
     const uint32_t tO = tmem + t_lane + static_cast<uint32_t>(L::kTmemO + s * D);
-    const float c = p.scale_log2;
-    const float tau = p.rescale_tau;
     uint32_t n_s = 0;
     bool ok = true;
 
@@ -271,82 +268,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < nT; ++j, ++n_s) {
         if (!wait_bar_warp(bar(L::S_FULL + s), n_s & 1, ctl)) { ok = false; break; }
         tc_fence_after();
-        uint32_t sr[8][16];
-#pragma unroll
-        for (int cc = 0; cc < 8; cc += 2) tmem_ld32(tS + cc * 16, sr[cc], sr[cc + 1]);
-        tmem_wait_ld();
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) reg_fence16(sr[cc]);
-
-        // mask: ragged key tail, and the causal diagonal (this CTA's rows;
-        // the pair's stage may reach one tile further than these rows need)
-        const int key0 = j * kBN;
-        const bool need_mask =
-            (key0 + kBN > p.Skv) || (p.causal && key0 + kBN - 1 > stage_row0 + off);
-        if (need_mask) {
-          int lim = p.Skv - 1 - key0;
-          if (p.causal) lim = min(lim, row_g + off - key0);
-#pragma unroll
-          for (int cc = 0; cc < 8; ++cc)
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-              if (cc * 16 + e > lim) sr[cc][e] = __float_as_uint(-INFINITY);
-        }
-        float mx[16];
-#pragma unroll
-        for (int g = 0; g < 16; ++g) {
-          const uint32_t* v = &sr[g >> 1][(g & 1) * 8];
-          float a = fmax3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
-          a = fmax3(a, __uint_as_float(v[3]), __uint_as_float(v[4]));
-          a = fmax3(a, __uint_as_float(v[5]), __uint_as_float(v[6]));
-          mx[g] = fmaxf(a, __uint_as_float(v[7]));
-        }
-        const float r0 = fmax3(mx[0], mx[1], mx[2]), r1 = fmax3(mx[3], mx[4], mx[5]);
-        const float r2 = fmax3(mx[6], mx[7], mx[8]), r3 = fmax3(mx[9], mx[10], mx[11]);
-        const float r4 = fmax3(mx[12], mx[13], mx[14]);
-        const float t_max = fmaxf(fmax3(r0, r1, r2), fmax3(r3, r4, mx[15])) * c;
-        const float m_new = t_max > m + tau ? t_max : m;
-        const float m_use = m_new == -INFINITY ? 0.f : m_new;
-        const float alpha = m_new == m ? 1.f : ex2_approx(m - m_use);
-        const float neg_m = -m_use;
-        float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const int col = h * 32 + q * 4;
-            uint32_t* v = &sr[col >> 4][col & 15];
-            float x0, x1, x2, x3;
-            ffma2(x0, x1, __uint_as_float(v[0]), __uint_as_float(v[1]), c, c, neg_m, neg_m);
-            ffma2(x2, x3, __uint_as_float(v[2]), __uint_as_float(v[3]), c, c, neg_m, neg_m);
-            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-            const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
-            fadd2(l0, l1, l0, l1, p0, p1);
-            fadd2(l2, l3, l2, l3, p2, p3);
-            pk[2 * q] = pack2<BF16>(p0, p1);
-            pk[2 * q + 1] = pack2<BF16>(p2, p3);
-          }
-          tmem_st16(tS + h * 16, pk);
-        }
-        l = l * alpha + ((l0 + l1) + (l2 + l3));
-        m = m_new;
-        // O_s *= alpha (rare); PV_s(j-1) has completed: S_FULL_s(j) was
-        // committed after it
-        if (j > 0 && (p.always_rescale || __any_sync(0xffffffffu, alpha != 1.f))) {
-#pragma unroll 1
-          for (int cc = 0; cc < D / 16; ++cc) {
-            uint32_t v[16];
-            tmem_ld16(tO + cc * 16, v);
-            tmem_wait_ld();
-            reg_fence16(v);
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-              v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-            tmem_st16(tO + cc * 16, v);
-          }
-        }
-        tmem_wait_st();
+        // this CTA's rows; the pair's stage may reach one tile further than
+        // they need (masked)
+        softmax_tile<D, BF16>(tS, tO, j * kBN, stage_row0, row_g, p, j > 0, m, l);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster_relaxed(bar_l(L::PV_READY + s));
@@ -399,30 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tO = tmem + t_lane + static_cast<uint32_t>(L::kTmemO + s * D);
         if (lane == 0) bulk_wait_group_read0();
         __syncwarp();
-#pragma unroll 1
-        for (int cc = 0; cc < D / 16; ++cc) {
-          uint32_t v[16];
-          if (have_o) {
-            tmem_ld16(tO + cc * 16, v);
-            tmem_wait_ld();
-            reg_fence16(v);
-          } else {
-#pragma unroll
-            for (int e = 0; e < 16; ++e) v[e] = 0u;
-          }
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int col = cc * 16 + h * 8;
-            const uint32_t w0 = pack2<BF16>(__uint_as_float(v[h * 8 + 0]) * inv_l, __uint_as_float(v[h * 8 + 1]) * inv_l);
-            const uint32_t w1 = pack2<BF16>(__uint_as_float(v[h * 8 + 2]) * inv_l, __uint_as_float(v[h * 8 + 3]) * inv_l);
-            const uint32_t w2 = pack2<BF16>(__uint_as_float(v[h * 8 + 4]) * inv_l, __uint_as_float(v[h * 8 + 5]) * inv_l);
-            const uint32_t w3 = pack2<BF16>(__uint_as_float(v[h * 8 + 6]) * inv_l, __uint_as_float(v[h * 8 + 7]) * inv_l);
-            const int box = col >> 6, chunk = (col & 63) >> 3;
-            st_shared_v4(stage_buf + static_cast<uint32_t>(box * L::kOutBox + lane * 128 +
-                                                           ((chunk ^ (lane & 7)) << 4)),
-                         w0, w1, w2, w3);
-          }
-        }
+        stage_o_rows<D, BF16>(tO, have_o, inv_l, stage_buf, L::kOutBox, lane);
         if (have_o) {
           tc_fence_before();
           __syncwarp();
@@ -687,7 +588,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // drain (leader): its barriers complete only when both CTAs' loads
-      // have landed; the follower exits after the final cluster barrier
+      // have landed; the follower exits after the final cluster barrier.
+      // After a watchdog abort the follower may have issued loads that the
+      // leader never armed; it cannot wait on them (their barrier is the
+      // leader's), so it gives them a bounded time to land before exiting.
+      if (!leader && *abort_flag) {
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 100000ull) __nanosleep(1000);
+      }
       if (leader) {
 #pragma unroll
         for (int s = 0; s < 2; ++s)

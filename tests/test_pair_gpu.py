@@ -113,3 +113,15 @@ def test_pair_watchdog_reports_timeout_and_context_survives():
         fa.fa_set_watchdog_ns(0)
     o, lse = run_kernel(q, k, v, False, flags=PAIR)
     _assert(check(q, k, v, o, lse, False, "bf16"))
+
+
+def test_pair_exact_running_max_mode():
+    """FA_FLAG_EXACT_MAX on pairs passes the gate, and rescaling on every
+    tile changes no bit."""
+    w = inputs.C2_X4_CAUSAL
+    q, k, v = w.make()
+    o1, l1 = run_kernel(q, k, v, w.causal, flags=PAIR | fa.FA_FLAG_EXACT_MAX)
+    _assert(check(q, k, v, o1, l1, w.causal, w.dtype))
+    o2, l2 = run_kernel(q, k, v, w.causal,
+                        flags=PAIR | fa.FA_FLAG_EXACT_MAX | fa.FA_FLAG_ALWAYS_RESCALE)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
