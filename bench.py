@@ -53,6 +53,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-gemm-ceiling", action="store_true")
+    ap.add_argument("--prefill-kernel", default="auto", choices=["auto", "single", "pair"],
+                    help="prefill kernel: the library's choice (default), single CTAs "
+                         "(FA_FLAG_SINGLE_CTA) or CTA pairs (FA_FLAG_PAIR)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--ref-seconds", type=float, default=120.0,
@@ -339,8 +342,13 @@ def bench_ours(args, w):
     stream = torch.cuda.current_stream(device)
     decode = w.Sq == 1
 
+    kflags = {"auto": 0, "single": fa.FA_FLAG_SINGLE_CTA, "pair": fa.FA_FLAG_PAIR}[args.prefill_kernel]
+
     def step():
-        fa.fa_fwd(dq, dk, dv, causal=w.causal, out=o, lse=lse, stream=stream)
+        if kflags:
+            fa.fa_fwd_ex(dq, dk, dv, causal=w.causal, flags=kflags, out=o, lse=lse, stream=stream)
+        else:
+            fa.fa_fwd(dq, dk, dv, causal=w.causal, out=o, lse=lse, stream=stream)
 
     launches_per_step = 1
     if decode:
@@ -394,11 +402,12 @@ def bench_ours(args, w):
     else:
         achieved = flops_step / launch_s / 1e12
         peak = float(peaks["bf16_tflops"])
+        pairs = fa.fa_prefill_uses_pairs(w.B, w.H, w.Sq, w.Skv, w.D, w.causal, kflags)
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": profiled_traffic("prefill", w.name),
+                "frac": achieved / peak,
+                "traffic": profiled_traffic("prefill_pair" if pairs else "prefill_single", w.name),
                 "peak_source": f"{peak_src} bf16_tflops (burst; dense fp16 has the same rate)",
-                "kernel": ("fa_prefill_pair_kernel (two-CTA clusters)"
-                           if fa.fa_prefill_uses_pairs(w.B, w.H, w.Sq, w.Skv, w.D, w.causal)
+                "kernel": ("fa_prefill_pair_kernel (two-CTA clusters)" if pairs
                            else "fa_prefill_kernel")}
 
     line = {
