@@ -125,3 +125,39 @@ def test_pair_exact_running_max_mode():
     o2, l2 = run_kernel(q, k, v, w.causal,
                         flags=PAIR | fa.FA_FLAG_EXACT_MAX | fa.FA_FLAG_ALWAYS_RESCALE)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_pair_concurrent_streams_bitwise_identical():
+    q, k, v = inputs.make_qkv(2, 8, 1024, 1024, 128, "bf16", 27)
+    dq, dk, dv = (t.cuda() for t in (q, k, v))
+    ref, lref = fa.fa_fwd_ex(dq, dk, dv, causal=True, flags=PAIR)
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    outs = []
+    for s in streams:
+        with torch.cuda.stream(s):
+            outs.append(fa.fa_fwd_ex(dq, dk, dv, causal=True, flags=PAIR, stream=s))
+    torch.cuda.synchronize()
+    for o, l in outs:
+        assert torch.equal(o, ref) and torch.equal(l, lref)
+    assert fa.fa_get_device_status() == fa.FA_OK
+
+
+def test_pair_scheduler_slots_wrap_around():
+    """1100 pair launches (more than the 1024 scheduler slots), interleaved
+    with single-CTA launches that share the slots: every launch claims every
+    item."""
+    q, k, v = inputs.make_qkv(2, 32, 1024, 512, 128, "bf16", 28)
+    dq, dk, dv = (t.cuda() for t in (q, k, v))
+    ref, lref = fa.fa_fwd_ex(dq, dk, dv, causal=True, flags=PAIR)
+    o, lse = torch.empty_like(ref), torch.empty_like(lref)
+    for i in range(1100):
+        if i % 100 == 99:
+            o.zero_()
+            lse.fill_(float("nan"))
+        fa.fa_fwd_ex(dq, dk, dv, causal=True, flags=PAIR, out=o, lse=lse)
+        if i % 7 == 3:
+            fa.fa_fwd_ex(dq, dk, dv, causal=True, flags=fa.FA_FLAG_SINGLE_CTA)
+        if i % 100 == 99:
+            torch.cuda.synchronize()
+            assert torch.equal(o, ref) and torch.equal(lse, lref), i
+    assert fa.fa_get_device_status() == fa.FA_OK
