@@ -388,24 +388,28 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int key0,
 template <int D, bool BF16>
 __device__ __forceinline__ void stage_o_rows(uint32_t tO, bool have_o, float inv_l,
                                              uint32_t stage_buf, int out_box_bytes, int lane) {
+  // 32 columns per tensor-memory round trip (a load and its wait take ~240
+  // cycles; this read gates the next item's first PV into O)
 #pragma unroll 1
-  for (int cc = 0; cc < D / 16; ++cc) {
-    uint32_t v[16];
+  for (int cc = 0; cc < D / 32; ++cc) {
+    uint32_t v[2][16];
     if (have_o) {
-      tmem_ld16(tO + cc * 16, v);
+      tmem_ld32(tO + cc * 32, v[0], v[1]);
       tmem_wait_ld();
-      reg_fence16(v);
+      reg_fence16(v[0]);
+      reg_fence16(v[1]);
     } else {  // no visible key: O = 0
 #pragma unroll
-      for (int e = 0; e < 16; ++e) v[e] = 0u;
+      for (int e = 0; e < 16; ++e) v[0][e] = v[1][e] = 0u;
     }
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int col = cc * 16 + h * 8;  // first column of this 16-byte chunk
-      const uint32_t w0 = pack2<BF16>(__uint_as_float(v[h * 8 + 0]) * inv_l, __uint_as_float(v[h * 8 + 1]) * inv_l);
-      const uint32_t w1 = pack2<BF16>(__uint_as_float(v[h * 8 + 2]) * inv_l, __uint_as_float(v[h * 8 + 3]) * inv_l);
-      const uint32_t w2 = pack2<BF16>(__uint_as_float(v[h * 8 + 4]) * inv_l, __uint_as_float(v[h * 8 + 5]) * inv_l);
-      const uint32_t w3 = pack2<BF16>(__uint_as_float(v[h * 8 + 6]) * inv_l, __uint_as_float(v[h * 8 + 7]) * inv_l);
+    for (int h = 0; h < 4; ++h) {
+      const uint32_t* x = &v[h >> 1][(h & 1) * 8];
+      const int col = cc * 32 + h * 8;  // first column of this 16-byte chunk
+      const uint32_t w0 = pack2<BF16>(__uint_as_float(x[0]) * inv_l, __uint_as_float(x[1]) * inv_l);
+      const uint32_t w1 = pack2<BF16>(__uint_as_float(x[2]) * inv_l, __uint_as_float(x[3]) * inv_l);
+      const uint32_t w2 = pack2<BF16>(__uint_as_float(x[4]) * inv_l, __uint_as_float(x[5]) * inv_l);
+      const uint32_t w3 = pack2<BF16>(__uint_as_float(x[6]) * inv_l, __uint_as_float(x[7]) * inv_l);
       const int box = col >> 6, chunk = (col & 63) >> 3;
       st_shared_v4(stage_buf + static_cast<uint32_t>(box * out_box_bytes + lane * 128 +
                                                      ((chunk ^ (lane & 7)) << 4)),
