@@ -366,16 +366,19 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int key0,
   // completed (the kernels commit S_FULL after it) and passes may_rescale =
   // false on an item's first tile, which has no O to rescale.
   if (may_rescale && (p.always_rescale || __any_sync(0xffffffffu, alpha != 1.f))) {
-#pragma unroll 1
+    // the row's S values are no longer needed: all D columns of O in one
+    // tensor-memory round trip (each load-and-wait costs ~240 cycles)
+    uint32_t v[D / 16][16];
+#pragma unroll
+    for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(tO + cc * 32, v[2 * cc], v[2 * cc + 1]);
+    tmem_wait_ld();
+#pragma unroll
     for (int cc = 0; cc < D / 16; ++cc) {
-      uint32_t v[16];
-      tmem_ld16(tO + cc * 16, v);
-      tmem_wait_ld();
-      reg_fence16(v);
+      reg_fence16(v[cc]);
 #pragma unroll
       for (int e = 0; e < 16; ++e)
-        v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-      tmem_st16(tO + cc * 16, v);
+        v[cc][e] = __float_as_uint(__uint_as_float(v[cc][e]) * alpha);
+      tmem_st16(tO + cc * 16, v[cc]);
     }
   }
   tmem_wait_st();
