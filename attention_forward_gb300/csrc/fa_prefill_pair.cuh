@@ -585,6 +585,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           const unsigned long long ticket = atomicAdd(p.sched, 1ull);
           const unsigned long long nidx = (gridDim.x >> 1) + ticket;
           idx = nidx < static_cast<unsigned long long>(p.n_items) ? static_cast<int>(nidx) : -1;
+          if (idx >= 0) {
+            // the next item's Q (all 512 rows, both CTAs' shares) into L2
+            // now: its loads can start only once this item's last QKs have
+            // read the Q buffers
+            const PairItem nx = get_pair_item(p, idx);
+#pragma unroll 1
+            for (int rb = 0; rb < kPairRows / kBM; ++rb)
+#pragma unroll
+              for (int box = 0; box < D / 64; ++box)
+                tma_prefetch_l2_3d(&tmQ, box * 64, nx.row0 + rb * kBM, nx.bh);
+          }
         }
       }
       // drain (leader): its barriers complete only when both CTAs' loads
