@@ -289,7 +289,11 @@ __device__ __forceinline__ int take_item(const volatile int* ring, uint32_t full
 // write P = 2^(c*s - m) as packed 16-bit pairs over the first 64 columns of S,
 // update the row sum l, and rescale this warp's rows of O (D columns at tO)
 // when one of them moved its reference max.  Ends with tcgen05.wait::st.
-template <int D, bool BF16>
+// kVoteFirst places the warp's vote on that rescale before the exponentials
+// rather than after them: the arithmetic is the same, only the instruction
+// schedule differs (measured faster for the single-CTA kernel, slower for
+// the CTA-pair kernel).
+template <int D, bool BF16, bool kVoteFirst = true>
 __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int key0, int stage_row0,
                                              int row_g, const PrefillParams& p, bool may_rescale,
                                              float& m, float& l) {
@@ -334,6 +338,13 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int key0,
   const float m_use = m_new == -INFINITY ? 0.f : m_new;
   const float alpha = m_new == m ? 1.f : ex2_approx(m - m_use);
   const float neg_m = -m_use;
+  // O *= alpha when a row of this warp moved its reference max (rare: tau
+  // keeps it still).  The caller guarantees that the previous PV into O has
+  // completed (the kernels commit S_FULL after it) and passes may_rescale =
+  // false on an item's first tile, which has no O to rescale.
+  bool rescale = false;
+  if constexpr (kVoteFirst)
+    rescale = may_rescale && (p.always_rescale || __any_sync(0xffffffffu, alpha != 1.f));
   // p = 2^(s*c - m) in four 32-column pieces: the argument as packed
   // fp32x2 FMAs, the row sum as packed fp32x2 adds; each piece is packed
   // to 16-bit pairs and stored over the first 64 columns of S_s (every S
@@ -361,11 +372,9 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int key0,
   }
   l = l * alpha + ((l0 + l1) + (l2 + l3));
   m = m_new;
-  // O *= alpha when a row of this warp moved its reference max (rare: tau
-  // keeps it still).  The caller guarantees that the previous PV into O has
-  // completed (the kernels commit S_FULL after it) and passes may_rescale =
-  // false on an item's first tile, which has no O to rescale.
-  if (may_rescale && (p.always_rescale || __any_sync(0xffffffffu, alpha != 1.f))) {
+  if constexpr (!kVoteFirst)
+    rescale = may_rescale && (p.always_rescale || __any_sync(0xffffffffu, alpha != 1.f));
+  if (rescale) {
     // the row's S values are no longer needed: all D columns of O in one
     // tensor-memory round trip (each load-and-wait costs ~240 cycles)
     uint32_t v[D / 16][16];

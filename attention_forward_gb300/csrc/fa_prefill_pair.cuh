@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         // this CTA's rows; the pair's stage may reach one tile further than
         // they need (masked)
-        softmax_tile<D, BF16>(tS, tO, j * kBN, stage_row0, row_g, p, j > 0, m, l);
+        softmax_tile<D, BF16, false>(tS, tO, j * kBN, stage_row0, row_g, p, j > 0, m, l);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster_relaxed(bar_l(L::PV_READY + s));
