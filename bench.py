@@ -235,11 +235,11 @@ class OracleSample:
     """The fp64 oracle timed on a row sample of the workload (host cores).
     The per-row cost is 4*Skv*D FLOPs (the visible keys for causal rows)."""
 
-    def __init__(self, w: inputs.Workload, seed: int = 0):
+    def __init__(self, w: inputs.Workload, seed: int = 0, nthreads: int = 0):
         import oracle
         self.oracle = oracle
         self.w = w
-        self.nthreads = oracle.default_threads()
+        self.nthreads = nthreads or oracle.default_threads()
         self.rng = np.random.default_rng(seed)
         heads = sorted(set(int(x) for x in self.rng.integers(0, w.B * w.H, size=4)))
         self.nh = len(heads)
@@ -264,6 +264,7 @@ class OracleSample:
 
     def rows_for(self, target_s: float) -> int:
         n = max(self.nthreads, 8)
+        self.run(n)  # the first call pays one-time costs: not a calibration point
         dt, _ = self.run(n)
         while dt < 0.25 and n < (1 << 20):
             n *= 4
@@ -275,9 +276,10 @@ class OracleSample:
                 f"{self.w.name}, fp64, {self.nthreads} threads")
 
 
-def oracle_rate(w: inputs.Workload, target_s: float):
-    """(TFLOP/s, cores, sample, seconds) of the oracle on about target_s of work."""
-    smp = OracleSample(w)
+def oracle_rate(w: inputs.Workload, target_s: float, nthreads: int = 0):
+    """(TFLOP/s, cores, sample, seconds) of the oracle on about target_s of
+    work, on nthreads host threads (0: all cores)."""
+    smp = OracleSample(w, nthreads=nthreads)
     n = smp.rows_for(target_s)
     dt, fl = smp.run(n)
     return fl / dt / 1e12, smp.nthreads, smp.describe(n), dt
@@ -383,7 +385,9 @@ def bench_ours(args, w):
         raise RuntimeError("kernel watchdog fired in the timed region")
 
     total_s = t_start.elapsed_time(t_end) / 1e3
-    launch_s = statistics.mean(a.elapsed_time(b) for a, b in ev) / 1e3
+    launch_ms = sorted(a.elapsed_time(b) for a, b in ev)
+    launch_s = statistics.mean(launch_ms) / 1e3
+    pct = lambda f: launch_ms[min(K - 1, int(f * K))]
     total_max = max_over_ranks(total_s, world, device)
     flops_step = w.flops()
     value = job_throughput(flops_step, K, world, total_max)
@@ -420,6 +424,8 @@ def bench_ours(args, w):
                           f"{'>' if 3 * dq.numel() * 2 > L2_BYTES else '<='} L2 129 MiB; no flush"),
         "roofline": roof,
         "gpu_launches": K * launches_per_step,
+        "step_ms": {"mean": launch_s * 1e3, "median": statistics.median(launch_ms),
+                    "p10": pct(0.10), "p90": pct(0.90), "source": "CUDA events around each step"},
         "clocks": sampler.summary(wall0, wall1),
     }
 
@@ -431,8 +437,11 @@ def bench_ours(args, w):
         line["frac_of_same_run_gemm"] = roof["achieved"] / g if not decode else None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         r, cores, sample, dt = oracle_rate(w, args.cpu_seconds)
+        r1, _, sample1, dt1 = oracle_rate(w, args.cpu_seconds / 2, nthreads=1)
         line["cpu_baseline"] = {"value": r, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                "sample": sample, "seconds": dt}
+                                "sample": sample, "seconds": dt,
+                                "one_core": {"value": r1, "unit": UNIT, "sample": sample1,
+                                             "seconds": dt1}}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
