@@ -53,10 +53,14 @@ __device__ unsigned g_status_word;
 
 // Slots of the prefill kernel's item scheduler (see PrefillParams::sched);
 // zero at load, and cleared again by the last CTA of every launch.
-__device__ unsigned long long g_sched[2 * fa::kSchedSlots];
+__device__ unsigned long long g_sched[2 * (fa::kSchedSlots + fa::kGraphSchedSlots)];
 // Prefill launches of this process, numbered to pick a scheduler slot: two
-// launches can share a slot only 1024 launches apart.
+// direct launches can share a slot only 1024 launches apart.
 std::atomic<unsigned> g_launch_seq{0};
+// Prefill launches captured into CUDA graphs: each takes a slot of its own
+// (a graph replays with the slot it was captured with, on any stream), out
+// of a pool of 4096 that direct launches never use.
+std::atomic<unsigned> g_capture_seq{0};
 
 constexpr int kMaxDevices = 64;
 constexpr unsigned long long kDefaultWatchdogNs = 1000000000ull;
@@ -175,6 +179,14 @@ fa_status_t encode_3d(CUtensorMap* m, const void* base, int D, int S, int BH,
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+// The scheduler slot of one prefill launch (see g_launch_seq, g_capture_seq).
+unsigned long long* sched_slot(const DeviceState& d, bool captured) {
+  const unsigned n = captured
+      ? fa::kSchedSlots + g_capture_seq.fetch_add(1) % fa::kGraphSchedSlots
+      : g_launch_seq.fetch_add(1) % fa::kSchedSlots;
+  return d.sched + 2 * static_cast<size_t>(n);
+}
+
 // fa_fwd's workspace for `stream` on this device, grown to `need` bytes.
 fa_status_t stream_workspace(DeviceState& d, cudaStream_t stream, size_t need, void** out) {
   std::lock_guard<std::mutex> lock(g_mu);
@@ -245,7 +257,8 @@ bool pair_by_default(int BH, int Sq, int Skv, int causal, int sm_count) {
 // query rows, a persistent grid of two-CTA clusters.
 fa_status_t run_prefill_pair(DeviceState& d, const void* q, const void* k, const void* v,
                              void* o, float* lse, int BH, int Sq, int Skv, float scale,
-                             int causal, bool bf16, unsigned flags, cudaStream_t stream) {
+                             int causal, bool bf16, unsigned flags, bool captured,
+                             cudaStream_t stream) {
   const int ti = bf16 ? 1 : 0;
   {
     std::lock_guard<std::mutex> lock(g_mu);
@@ -284,7 +297,7 @@ fa_status_t run_prefill_pair(DeviceState& d, const void* q, const void* k, const
   const long long n_items = static_cast<long long>(p.n_qtiles) * BH;
   if (n_items > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
   p.n_items = static_cast<int>(n_items);
-  p.sched = d.sched + 2 * (g_launch_seq.fetch_add(1) % fa::kSchedSlots);
+  p.sched = sched_slot(d, captured);
   const int n_pairs = static_cast<int>(std::min<long long>(n_items, d.pair_slots[ti]));
   if (fa::launch_prefill_pair(bf16, tq, tk, tv, to, p, n_pairs, stream) != cudaSuccess)
     return FA_ERR_CUDA;
@@ -295,7 +308,7 @@ fa_status_t run_prefill(DeviceState& d, const void* q, const void* k, const void
                         void* o, float* lse, int B, int H, int Sq, int Skv, int D,
                         float scale, int causal, bool bf16, unsigned flags,
                         int num_splits, void* ws, size_t ws_bytes, bool own_ws,
-                        cudaStream_t stream) {
+                        bool captured, cudaStream_t stream) {
   fa_status_t st = get_encoder();
   if (st != FA_OK) return st;
   {
@@ -314,7 +327,7 @@ fa_status_t run_prefill(DeviceState& d, const void* q, const void* k, const void
   if (D == 128 && num_splits <= 1 && !(flags & FA_FLAG_SINGLE_CTA) &&
       ((flags & FA_FLAG_PAIR) || pair_by_default(BH, Sq, Skv, causal, d.sm_count)))
     return run_prefill_pair(d, q, k, v, o, lse, BH, Sq, Skv, scale, causal, bf16, flags,
-                            stream);
+                            captured, stream);
   CUtensorMap tq, tk, tv, to;
   if ((st = encode_3d(&tq, q, D, Sq, BH, fa::kBM, bf16)) != FA_OK) return st;
   if ((st = encode_3d(&tk, k, D, Skv, BH, fa::kBN, bf16)) != FA_OK) return st;
@@ -362,7 +375,7 @@ fa_status_t run_prefill(DeviceState& d, const void* q, const void* k, const void
   const long long n_items = static_cast<long long>(p.n_qtiles) * BH * n_splits;
   if (n_items > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
   p.n_items = static_cast<int>(n_items);
-  p.sched = d.sched + 2 * (g_launch_seq.fetch_add(1) % fa::kSchedSlots);
+  p.sched = sched_slot(d, captured);
   // persistent: one CTA per SM (the kernel's shared memory allows no second)
   const int grid = static_cast<int>(std::min<long long>(n_items, d.sm_count > 0 ? d.sm_count : 1));
   if (fa::launch_prefill(D, bf16, tq, tk, tv, to, p, grid, stream) != cudaSuccess)
@@ -459,6 +472,19 @@ fa_status_t forward(const void* q, const void* k, const void* v, void* o, float*
   if (num_splits < 0) return FA_ERR_INVALID_ARG;
   DeviceState* d = nullptr;
   if ((st = current_device(&d, nullptr)) != FA_OK) return st;
+  // A call captured into a CUDA graph may be replayed on any stream, so it
+  // takes a scheduler slot of its own and no library-owned workspace: the
+  // shapes the library would split run unsplit (a caller's workspace, passed
+  // to fa_fwd_ex, keeps the split).
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return FA_ERR_CUDA;
+  const bool captured = cap != cudaStreamCaptureStatusNone;
+  if (captured && own_ws) {
+    own_ws = false;
+    ws = nullptr;
+    ws_bytes = 0;
+    if (Sq == 1) num_splits = 1;
+  }
   const bool bf16 = dtype == FA_BF16;
   // one query row per head: every key is visible (causal or not), and the
   // split-KV decode kernel serves it
@@ -466,7 +492,7 @@ fa_status_t forward(const void* q, const void* k, const void* v, void* o, float*
     return run_decode(*d, q, k, v, o, lse, B * H, Skv, D, scale, bf16, num_splits, ws,
                       ws_bytes, own_ws, stream);
   return run_prefill(*d, q, k, v, o, lse, B, H, Sq, Skv, D, scale, causal, bf16, flags,
-                     num_splits, ws, ws_bytes, own_ws, stream);
+                     num_splits, ws, ws_bytes, own_ws, captured, stream);
 }
 
 }  // namespace

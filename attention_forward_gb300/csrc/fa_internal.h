@@ -22,8 +22,11 @@ constexpr int kThreads = 512;  // 4 warpgroups
 // Dynamic item scheduler: slots of a static device array, one per launch
 // (chosen round-robin by the host), two words each: [0] = items claimed,
 // [1] = CTAs finished.  Both are zero when a launch starts: the launch's
-// last CTA clears them.
+// last CTA clears them.  kSchedSlots slots rotate among direct launches;
+// kGraphSchedSlots more go, one each, to launches captured into CUDA graphs,
+// which keep their slot for every replay.
 constexpr int kSchedSlots = 1024;
+constexpr int kGraphSchedSlots = 4096;
 
 struct PrefillParams {
   float* lse;                 // [B*H, Sq]

@@ -36,6 +36,18 @@
  * watchdog limit (default 1 s) makes the kernel stop, release what it holds
  * and record FA_ERR_TIMEOUT in a device status word, which
  * fa_get_device_status() reports.  No entry point prints, throws or aborts.
+ *
+ * CUDA graphs: fa_fwd, fa_fwd_ex and fa_fwd_host may be called while
+ * `stream` is being captured; the graph then replays the same launches, on
+ * any stream.  A captured call uses no library-owned workspace, so the
+ * shapes fa_fwd would split (few query tiles, or decode) run unsplit there;
+ * fa_fwd_ex with a caller workspace keeps the split, and the workspace is
+ * then the graph's to keep.  Each captured prefill takes one of 4096
+ * scheduler slots reserved for captures, which direct launches never use:
+ * replays of one graph run in stream order, and replays of graphs captured
+ * more than 4096 prefill calls apart must not overlap.
+ * fa_get_device_status synchronises and cannot be captured;
+ * fa_fwd_decode_static's scratch makes overlapping replays race.
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H
