@@ -245,12 +245,12 @@ size_t prefill_ws_bytes(int BH, int Sq, int D, int n_splits) {
 }
 
 // The library runs prefill on CTA pairs where they measured faster than
-// single CTAs on GB300: long rows (non-causal from 2048 queries and keys,
-// causal from 16384), and at least one 512-row item per pair of SMs.
+// single CTAs on GB300: long rows (non-causal from 1024 queries and keys,
+// causal from 8192), and at least one 512-row item per pair of SMs.
 bool pair_by_default(int BH, int Sq, int Skv, int causal, int sm_count) {
   const long long items = static_cast<long long>(BH) * ((Sq + 511) / 512);
   if (items < (sm_count > 0 ? sm_count / 2 : 76)) return false;
-  return causal ? Sq >= 16384 : (Sq >= 2048 && Skv >= 2048);
+  return causal ? Sq >= 8192 : (Sq >= 1024 && Skv >= 1024);
 }
 
 // Prefill by CTA pairs (FA_FLAG_PAIR, D = 128, whole key range): items of 512

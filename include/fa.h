@@ -94,7 +94,7 @@ typedef enum {
                                         ignored otherwise.  Without this flag
                                         or FA_FLAG_SINGLE_CTA the library
                                         uses pairs for long rows (non-causal
-                                        Sq, Skv >= 2048; causal Sq >= 16384)
+                                        Sq, Skv >= 1024; causal Sq >= 8192)
                                         with at least one 512-row item per
                                         two SMs                             */
 #define FA_FLAG_SINGLE_CTA 0x10u     /* prefill: never use CTA pairs        */

@@ -60,8 +60,11 @@ def test_pair_selection_without_a_gpu(lib):
     assert not fa.fa_prefill_uses_pairs(1, 1, 300, 300, 128, False, P, num_splits=2)
     assert fa.fa_prefill_uses_pairs(4, 16, 4096, 4096, 128, False)
     assert fa.fa_prefill_uses_pairs(8, 16, 2048, 2048, 128, False)
-    assert not fa.fa_prefill_uses_pairs(16, 16, 1024, 1024, 128, False)
-    assert not fa.fa_prefill_uses_pairs(1, 16, 8192, 8192, 128, True)
+    assert fa.fa_prefill_uses_pairs(16, 16, 1024, 1024, 128, False)
+    assert not fa.fa_prefill_uses_pairs(32, 16, 512, 512, 128, False)
+    assert not fa.fa_prefill_uses_pairs(16, 16, 1024, 512, 128, False)
+    assert not fa.fa_prefill_uses_pairs(4, 16, 4096, 4096, 128, True)
+    assert fa.fa_prefill_uses_pairs(2, 16, 8192, 8192, 128, True)
     assert fa.fa_prefill_uses_pairs(1, 16, 16384, 16384, 128, True)
     assert not fa.fa_prefill_uses_pairs(1, 1, 4096, 4096, 128, False)  # 8 items
 
