@@ -5,7 +5,7 @@ two-reference gate: an output passes iff its worst absolute error against the
 high-precision oracle is at most twice the worst error of a same-precision
 reference plus a small constant; the page derived those constants empirically
 over thousands of configurations.  The bound used here keeps that shape with
-the constants this build is held to:
+the constants the CUDA path is held to:
 
     err_O  = max |O_kernel - O_oracle|          over every compared element
     floor  = max |O_floor  - O_oracle|          (fp32 accumulation on the
