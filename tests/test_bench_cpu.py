@@ -77,3 +77,21 @@ def test_reference_arm_other_ranks_exit_without_work():
                         "reference", "--steps", "1", "--warmup", "0"],
                        capture_output=True, text=True, timeout=300, cwd=ROOT, env=env)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_kernel_fingerprint_covers_device_code_only(tmp_path, monkeypatch):
+    """The fingerprint that keys the committed ncu traffic records changes with
+    the device code and launch wrappers, not with the host-side dispatch."""
+    import shutil
+    src = os.path.join(ROOT, "attention_forward_gb300", "csrc")
+    dst = tmp_path / "attention_forward_gb300" / "csrc"
+    shutil.copytree(src, dst)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    f0 = bench.kernel_fingerprint()
+    assert f0 == bench.kernel_fingerprint()
+    api = dst / "fa_api.cu"
+    api.write_text(api.read_text() + "\n// a host-side edit\n")
+    assert bench.kernel_fingerprint() == f0
+    dev = dst / "fa_prefill_pair.cuh"
+    dev.write_text(dev.read_text() + "\n// a device-side edit\n")
+    assert bench.kernel_fingerprint() != f0
