@@ -65,3 +65,19 @@ def test_row_max_rising_across_tiles(kernel, exact):
     # rescaling on every tile changes no bit
     o2, l2 = run_kernel(q, k, v, False, flags=f | fa.FA_FLAG_ALWAYS_RESCALE)
     assert torch.equal(o, o2) and torch.equal(lse, l2)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("scale", [1.0, 1e-3], ids=["sharp", "flat"])
+@pytest.mark.parametrize("shape", [(2, 4, 1, 5000), (1, 2, 256, 8192)], ids=["decode", "split_prefill"])
+def test_extreme_scales_through_key_splits(shape, scale, D):
+    """Decode and a prefill with few query tiles split their keys and merge
+    the ranges' (O, LSE) by LSE weights: a sharp softmax puts nearly all the
+    weight in one range.  V scaled by 1/4 as in test_extreme_scales."""
+    B, H, Sq, Skv = shape
+    assert fa.fa_workspace_bytes(B, H, Sq, Skv, D) > 0  # the library splits these
+    q, k, v = inputs.make_qkv(B, H, Sq, Skv, D, "bf16", 53)
+    v = v * 0.25
+    o, lse = run_kernel(q, k, v, False, scale=scale)
+    r = check(q, k, v, o, lse, False, "bf16", scale=scale)
+    assert r.passed, str(r)
