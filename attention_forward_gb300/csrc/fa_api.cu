@@ -13,6 +13,7 @@
 #include <vector>
 
 #include "../../include/fa.h"
+#include "fa_host.h"
 #include "fa_internal.h"
 #include "fa_launch.h"
 
@@ -68,6 +69,7 @@ std::atomic<unsigned long long> g_watchdog_ns{kDefaultWatchdogNs};
 
 struct DeviceState {
   bool probed = false;
+  unsigned long long ctx_id = 0;  // the context the addresses below belong to
   fa_status_t usable = FA_ERR_UNSUPPORTED;
   int sm_count = 0;
   unsigned* status = nullptr;
@@ -78,8 +80,8 @@ struct DeviceState {
   // (two-CTA clusters) that fit on the device at once, per dtype
   bool pair_checked[2] = {};
   int pair_slots[2] = {};  // 0: not usable
-  // fa_fwd's workspaces for split partials, one per stream (calls on one
-  // stream run in order; calls on different streams may overlap)
+  // fa_fwd's workspaces for split partials, one per stream handle (calls on
+  // one stream run in order; calls on different streams may overlap)
   struct StreamWorkspace {
     cudaStream_t stream;
     void* ptr;
@@ -92,6 +94,9 @@ std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_get_id = nullptr;
 
 fa_status_t get_encoder() {
   static std::once_flag once;
@@ -106,13 +111,19 @@ fa_status_t get_encoder() {
   return g_encode ? FA_OK : FA_ERR_CUDA;
 }
 
-// Current device's state; checks compute capability 10.3 once.
+// Current device's state; checks compute capability 10.3 once per context.
+// A device whose context changed since the last probe (cudaDeviceReset makes
+// a new primary context) is probed again: the static arrays' addresses are
+// looked up anew, and the workspaces of the old context, which went away
+// with it, are forgotten.
 fa_status_t current_device(DeviceState** out, int* dev_out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+  const unsigned long long ctx = fa::context_id();
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceState& d = g_dev[dev];
+  if (d.probed && d.usable == FA_OK && ctx != d.ctx_id) d = DeviceState{};
   if (!d.probed) {
     int major = 0, minor = 0, sms = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
@@ -128,9 +139,12 @@ fa_status_t current_device(DeviceState** out, int* dev_out) {
       void* sched = nullptr;
       if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess ||
           cudaGetSymbolAddress(&sched, g_sched) != cudaSuccess) {
+        cudaGetLastError();  // leave no pending error behind
         d.probed = false;
         return FA_ERR_CUDA;
       }
+      // the lookup made the device's context current if it was not yet
+      d.ctx_id = fa::context_id();
       d.status = static_cast<unsigned*>(addr);
       d.sched = static_cast<unsigned long long*>(sched);
       d.usable = FA_OK;
@@ -497,6 +511,47 @@ fa_status_t forward(const void* q, const void* k, const void* v, void* o, float*
 
 }  // namespace
 
+namespace fa {
+
+unsigned long long context_id() {
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q{};
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!g_ctx_current || !g_ctx_get_id || g_ctx_current(&ctx) != CUDA_SUCCESS || !ctx ||
+      g_ctx_get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+fa_status_t check_device() {
+  DeviceState* d = nullptr;
+  return current_device(&d, nullptr);
+}
+
+fa_status_t check_call(const void* q, const void* k, const void* v, const void* o,
+                       const void* lse, int B, int H, int Sq, int Skv, int D,
+                       float scale, int dtype) {
+  const fa_status_t st = validate(q, k, v, o, lse, B, H, Sq, Skv, D, scale, dtype);
+  if (st != FA_OK) return st;
+  DeviceState* d = nullptr;
+  return current_device(&d, nullptr);
+}
+
+}  // namespace fa
+
 extern "C" {
 
 fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -591,6 +646,19 @@ fa_status_t fa_get_device_status(fa_stream_t stream) {
   return word == 0 ? FA_OK : static_cast<fa_status_t>(word);
 }
 
+fa_status_t fa_release_workspaces(void) {
+  DeviceState* d = nullptr;
+  const fa_status_t st = current_device(&d, nullptr);
+  if (st != FA_OK) return st;
+  if (cudaDeviceSynchronize() != cudaSuccess) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  fa_status_t out = FA_OK;
+  for (auto& w : d->workspaces)
+    if (cudaFree(w.ptr) != cudaSuccess) out = FA_ERR_CUDA;
+  d->workspaces.clear();
+  return out;
+}
+
 void fa_set_watchdog_ns(unsigned long long ns) {
   g_watchdog_ns.store(ns ? ns : kDefaultWatchdogNs);
 }
@@ -619,6 +687,6 @@ int fa_prefill_uses_pairs(int B, int H, int Sq, int Skv, int D, int causal, unsi
   return pair_by_default(B * H, Sq, Skv, causal, sms) ? 1 : 0;
 }
 
-int fa_version(void) { return 10100; }
+int fa_version(void) { return 10200; }
 
 }  // extern "C"

@@ -16,6 +16,7 @@
 #include <mutex>
 
 #include "../../include/fa.h"
+#include "fa_host.h"
 
 namespace {
 
@@ -25,23 +26,35 @@ static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
+// The scratch's device address per device, with the context it belongs to.
+struct ScratchAddr {
+  unsigned long long ctx;
+  void* ptr;
+};
+ScratchAddr g_scratch[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device, looked up once
-// per device.  In host code the array's name is only a host-side stand-in,
-// so the address must come from cudaGetSymbolAddress.
+// Device address of the scratch array on the current device.  In host code
+// the array's name is only a host-side stand-in, so the address comes from
+// cudaGetSymbolAddress: looked up once per device (with that device
+// current), and again if the device's context has changed since (after
+// cudaDeviceReset the module, and the array with it, is loaded anew).
 fa_status_t scratch_for_current_device(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+  const unsigned long long ctx = fa::context_id();
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_ptr[dev]) {
+  ScratchAddr& a = g_scratch[dev];
+  if (!a.ptr || a.ctx != ctx) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || !p)
+    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || !p) {
+      cudaGetLastError();  // leave no pending error behind
+      a = ScratchAddr{0, nullptr};
       return FA_ERR_CUDA;
-    g_scratch_ptr[dev] = p;
+    }
+    a = ScratchAddr{ctx, p};
   }
-  *out = g_scratch_ptr[dev];
+  *out = a.ptr;
   return FA_OK;
 }
 
@@ -52,9 +65,10 @@ extern "C" fa_status_t fa_fwd_decode_static(const void* q, const void* k,
                                             int B, int H, int Skv, int D,
                                             float scale, int dtype,
                                             fa_stream_t stream) {
-  if (B < 1 || H < 1 || Skv < 1) return FA_ERR_INVALID_ARG;
-  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
-  if (static_cast<long long>(B) * H >= 65536) return FA_ERR_INVALID_ARG;
+  // the arguments and the device first (an unsupported device gets
+  // FA_ERR_UNSUPPORTED, as from fa_fwd), then the scratch's capacity
+  const fa_status_t chk = fa::check_call(q, k, v, o, lse, B, H, 1, Skv, D, scale, dtype);
+  if (chk != FA_OK) return chk;
   // the partials of the library's split choice must fit the static array
   const size_t need = fa_workspace_bytes(B, H, 1, Skv, D, 0);
   if (need > kScratchBytes) return FA_ERR_WORKSPACE;

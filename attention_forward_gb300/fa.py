@@ -65,6 +65,8 @@ def load() -> ctypes.CDLL:
     L.fa_fwd_decode_static.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, cf,
                                        ci, vp]
     L.fa_fwd_decode_static.restype = ci
+    L.fa_release_workspaces.argtypes = []
+    L.fa_release_workspaces.restype = ci
     L.fa_get_device_status.argtypes = [vp]
     L.fa_get_device_status.restype = ci
     L.fa_set_watchdog_ns.argtypes = [ctypes.c_ulonglong]
@@ -73,6 +75,8 @@ def load() -> ctypes.CDLL:
     L.fa_status_string.restype = ctypes.c_char_p
     L.fa_prefill_uses_pairs.argtypes = [ci, ci, ci, ci, ci, ci, ctypes.c_uint, ci]
     L.fa_prefill_uses_pairs.restype = ci
+    L.fa_ex2_approx.argtypes = [vp, vp, ci, vp]
+    L.fa_ex2_approx.restype = ci
     L.fa_version.argtypes = []
     L.fa_version.restype = ci
     _lib = L
@@ -203,6 +207,11 @@ def fa_fwd_decode_static(q, k, v, scale: float | None = None, out=None,
     return out, lse
 
 
+def fa_release_workspaces() -> None:
+    """Synchronises the device and frees the workspaces fa_fwd keeps for it."""
+    _check(load().fa_release_workspaces(), "fa_release_workspaces")
+
+
 def fa_get_device_status(stream=None) -> int:
     """Synchronises the stream; returns and clears the device status word."""
     return int(load().fa_get_device_status(_stream_handle(stream)))
@@ -220,6 +229,17 @@ def fa_prefill_uses_pairs(B: int, H: int, Sq: int, Skv: int, D: int, causal: boo
                           flags: int = 0, num_splits: int = 0) -> bool:
     return bool(load().fa_prefill_uses_pairs(B, H, Sq, Skv, D, int(bool(causal)), flags,
                                               num_splits))
+
+
+def fa_ex2_approx(x, stream=None):
+    """2^x on the device with the kernels' exponential instruction (x: a
+    contiguous float32 CUDA tensor).  Returns a new tensor."""
+    if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous float32 CUDA tensor")
+    y = torch.empty_like(x)
+    _check(load().fa_ex2_approx(x.data_ptr(), y.data_ptr(), x.numel(),
+                                _stream_handle(stream)), "fa_ex2_approx")
+    return y
 
 
 def fa_version() -> int:

@@ -110,9 +110,10 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-# Host-side dispatch only (argument checks, the choice of kernel and split,
-# workspaces): not part of what a kernel's counters depend on.
-_HOST_ONLY = {"fa_api.cu", "fa_noalloc.cu"}
+# Host-side dispatch (argument checks, the choice of kernel and split,
+# workspaces) and the device self-check: not part of what the attention
+# kernels' counters depend on.
+_HOST_ONLY = {"fa_api.cu", "fa_noalloc.cu", "fa_host.h", "fa_diag.cu"}
 
 
 def kernel_fingerprint() -> str:

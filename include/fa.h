@@ -48,6 +48,11 @@
  * more than 4096 prefill calls apart must not overlap.
  * fa_get_device_status synchronises and cannot be captured;
  * fa_fwd_decode_static's scratch makes overlapping replays race.
+ *
+ * Device reset: the library keeps, per device, the addresses of its static
+ * device arrays and its workspaces.  After cudaDeviceReset (a new primary
+ * context) the next call looks the addresses up again and forgets the
+ * workspaces, which went away with the old context.
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H
@@ -117,8 +122,14 @@ typedef enum {
  * each item are split into ranges whose fp32 partials a combine kernel
  * merges.  Decode (Sq == 1): split-KV kernel plus combine kernel.  The
  * partials go to a workspace that the library allocates on the first call
- * that needs one on each device and keeps until process exit (use fa_fwd_ex
- * to supply your own).
+ * that needs one, one per (device, stream handle), and keeps until
+ * fa_release_workspaces() or process exit (use fa_fwd_ex to supply your
+ * own).  A call that needs a larger workspace than its stream's frees the
+ * old one first (cudaFree, which synchronises the device) and allocates
+ * the new one.  The cache is keyed on the stream handle: a stream created
+ * after another was destroyed may receive the same handle, and would then
+ * share that stream's workspace, so call fa_release_workspaces() after
+ * destroying streams that fa_fwd used.
  * Returns FA_OK once the work is enqueued.
  */
 fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o,
@@ -191,9 +202,11 @@ fa_status_t fa_fwd_host(const void *q_h, const void *k_h, const void *v_h,
  * the library's choice, fa_workspace_bytes(B, H, 1, Skv, D, 0) gives the
  * exact figure); a shape that needs more returns FA_ERR_WORKSPACE before
  * anything is launched.  Nothing in the array has to start at zero.
- * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any stream
- * capture.  Calls share the one array: two calls whose work overlaps on the
+ * The arguments and the device are checked first, exactly as by fa_fwd
+ * (an unsupported device returns FA_ERR_UNSUPPORTED), then the scratch's
+ * capacity.  The first call on a device looks up the array's device address
+ * (once per device, with that device current, and again after the device's
+ * context was reset); make that first call before any stream capture.  Calls share the one array: two calls whose work overlaps on the
  * GPU (different streams, or different host threads) race and corrupt each
  * other's results.  Allocates nothing.
  */
@@ -204,12 +217,32 @@ fa_status_t fa_fwd_decode_static(const void *q, const void *k, const void *v,
                                  fa_stream_t stream);
 
 /*
+ * fa_release_workspaces -- frees the workspaces that fa_fwd keeps for split
+ * partials on the current device (one per stream handle it was called
+ * with), after synchronising the device.  The next fa_fwd that needs one
+ * allocates it again.  Returns FA_ERR_CUDA if the synchronisation or a free
+ * failed (the cache is emptied either way).
+ */
+fa_status_t fa_release_workspaces(void);
+
+/*
  * fa_get_device_status -- synchronises `stream`, then returns and clears the
  * device status word of the current device: FA_OK, or FA_ERR_TIMEOUT if a
  * kernel's bounded wait ran out since the last call.  FA_ERR_CUDA if the
  * synchronisation itself failed.
  */
 fa_status_t fa_get_device_status(fa_stream_t stream);
+
+/*
+ * fa_ex2_approx -- y[i] = 2^x[i] for i < n, computed on the device by the
+ * instruction the softmax of every kernel uses for its exponentials
+ * (ex2.approx.ftz.f32: subnormal results flush to +0).  A self-check of the
+ * values the kernels rely on: masked scores are -inf and must give +0, the
+ * row maximum gives 2^0 = 1 ("The FA5090 Optimization Journey", section 2.6,
+ * asserts both on the device).  x and y are device pointers to n fp32
+ * values, 4-byte aligned, 1 <= n <= 2^28; asynchronous on `stream`.
+ */
+fa_status_t fa_ex2_approx(const float *x, float *y, int n, fa_stream_t stream);
 
 /* Watchdog limit for every kernel-side wait, in nanoseconds (default 1e9).
  * Applies to launches made after the call.  0 restores the default. */

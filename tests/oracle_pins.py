@@ -203,3 +203,127 @@ def pin_fully_masked(lib):
 ALL_PINS = [pin_library_sdpa, pin_q_zero, pin_causal_row0, pin_dominant_key,
             pin_probs, pin_shift_invariance, pin_single_key_and_two_keys,
             pin_heads_independent, pin_rows_path, pin_fully_masked]
+
+
+# ------------------------------------------------------------------ floor
+#
+# The fp32 same-precision floor (``floor_attention_rows``) sets half of the
+# parity bound, so a mistake that inflates its error would loosen the gate.
+# Its definition: fp32 scores, fp32 softmax with expf, the normalised P
+# rounded to the 16-bit input format, fp32 P.V, O rounded to the format
+# (round to nearest even); LSE = m + ln l in fp32.
+
+_TORCH_FMT = {oracle.FMT_BF16: torch.bfloat16, oracle.FMT_F16: torch.float16}
+
+
+def _to_fmt(x, fmt):
+    """Round to the 16-bit format through torch's cast (not the oracle's)."""
+    return torch.as_tensor(np.asarray(x, np.float32)).to(_TORCH_FMT[fmt]).float().numpy()
+
+
+def _fmt_inputs(shape, fmt, scale=1.0):
+    return _to_fmt(RNG.standard_normal(shape) * scale, fmt)
+
+
+def _fmt_ulp(x, fmt):
+    """Spacing of the 16-bit format at |x| (normal range)."""
+    mant, emin = (7, -126) if fmt == oracle.FMT_BF16 else (10, -14)
+    e = np.floor(np.log2(np.maximum(np.abs(x), 2.0 ** emin)))
+    return 2.0 ** (e - mant)
+
+
+def pin_floor_library_path(lib):
+    """The floor against torch's own fp32 CPU routines on the same 16-bit
+    inputs: fp32 matmul for the scores, torch.softmax, P cast to the format,
+    fp32 matmul with V, O cast to the format, torch.logsumexp for LSE.  The
+    two differ only in fp32 summation order, which moves O by at most one
+    unit of the format and almost never across a rounding boundary; LSE
+    agrees to fp32 rounding."""
+    cases = [(1, 2, 96, 160, 64, False, oracle.FMT_BF16, 1.0),
+             (1, 2, 96, 160, 64, True, oracle.FMT_BF16, 1.0),
+             (1, 2, 80, 80, 32, True, oracle.FMT_F16, 1.0),
+             (1, 1, 64, 200, 16, False, oracle.FMT_F16, 3.0)]
+    for B, H, Sq, Skv, D, causal, fmt, mult in cases:
+        q = _fmt_inputs((B, H, Sq, D), fmt, mult)
+        k = _fmt_inputs((B, H, Skv, D), fmt, mult)
+        v = _fmt_inputs((B, H, Skv, D), fmt)
+        scale = float(np.float32(D ** -0.5))
+        of, lf = oracle.floor_attention(q, k, v, scale, causal, fmt, nthreads=2,
+                                        lib=lib)
+        tq, tk, tv = (torch.from_numpy(x) for x in (q, k, v))
+        s = torch.matmul(tq, tk.transpose(-1, -2)) * scale
+        m = torch.from_numpy(_mask(Sq, Skv, causal))
+        s = s.masked_fill(~m, float("-inf"))
+        live = m.any(dim=1).numpy()
+        p = torch.softmax(s, dim=-1).to(_TORCH_FMT[fmt]).float()
+        o = torch.matmul(p, tv).to(_TORCH_FMT[fmt]).float().numpy()
+        lse = torch.logsumexp(s, dim=-1).numpy()
+        of_l, o_l = of[:, :, live], o[:, :, live]
+        diff = np.abs(of_l - o_l)
+        # a P value next to a rounding boundary of the format may round the
+        # other way in torch (its softmax multiplies by 1/l), which moves
+        # that row's O by a unit of P: allow it on a few rows
+        rows_off = np.any(diff > _fmt_ulp(o_l, fmt) * 1.0001, axis=-1)
+        assert np.mean(rows_off) <= 0.03, (Sq, Skv, causal, fmt, np.mean(rows_off))
+        assert np.mean(diff == 0.0) >= 0.99, np.mean(diff == 0.0)
+        assert np.abs(lf[:, :, live] - lse[:, :, live]).max() < 4e-6
+
+
+def pin_floor_q_zero_closed_form(lib):
+    """Q = 0: every visible score is exactly 0, expf(0) = 1, l = n, so the
+    floor's P is 1/n rounded to fp32 and then to the format, and with small
+    integer V every fp32 sum is exact: O_i = fmt(P * sum of the visible V
+    rows), LSE_i = ln n."""
+    for fmt in (oracle.FMT_BF16, oracle.FMT_F16):
+        Sq = Skv = 40
+        D = 8
+        q = np.zeros((1, 1, Sq, D), np.float32)
+        k = _fmt_inputs((1, 1, Skv, D), fmt)
+        v = RNG.integers(-8, 9, size=(1, 1, Skv, D)).astype(np.float32)
+        of, lf = oracle.floor_attention(q, k, v, 0.125, True, fmt, lib=lib)
+        for i in range(Sq):
+            n = i + 1
+            p = float(_to_fmt(np.float32(1.0) / np.float32(n), fmt))
+            expect = _to_fmt(p * v[0, 0, :n].astype(np.float64).sum(axis=0), fmt)
+            assert np.array_equal(of[0, 0, i], expect), (fmt, i)
+            assert abs(float(lf[0, 0, i]) - math.log(n)) < 2e-6
+
+
+def pin_floor_single_key_exact(lib):
+    """One visible key (causal row 0): P = 1 exactly, so O_0 = V_0 exactly
+    and LSE_0 = the fp32 score."""
+    for fmt in (oracle.FMT_BF16, oracle.FMT_F16):
+        q = _fmt_inputs((1, 1, 4, 64), fmt)
+        k = _fmt_inputs((1, 1, 4, 64), fmt)
+        v = _fmt_inputs((1, 1, 4, 64), fmt)
+        of, lf = oracle.floor_attention(q, k, v, 0.125, True, fmt, lib=lib)
+        assert np.array_equal(of[0, 0, 0], v[0, 0, 0])
+        s00 = 0.125 * float(q[0, 0, 0].astype(np.float64) @ k[0, 0, 0].astype(np.float64))
+        assert abs(float(lf[0, 0, 0]) - s00) < 1e-5
+
+
+def pin_floor_output_on_grid(lib):
+    """Every floor output is a value of the 16-bit format (the output is
+    rounded once at the end)."""
+    for fmt in (oracle.FMT_BF16, oracle.FMT_F16):
+        q, k, v = (_fmt_inputs((1, 2, 50, 32), fmt) for _ in range(3))
+        of, _ = oracle.floor_attention(q, k, v, 32 ** -0.5, False, fmt, lib=lib)
+        assert np.array_equal(of, _to_fmt(of, fmt))
+
+
+def pin_floor_within_oracle_rounding(lib):
+    """Against the fp64 oracle the floor errs by the 16-bit rounding of O and
+    P: a few units of the format, and not zero (it does round)."""
+    for fmt, u in ((oracle.FMT_BF16, 2.0 ** -8), (oracle.FMT_F16, 2.0 ** -11)):
+        q, k, v = (_fmt_inputs((1, 2, 120, 64), fmt) for _ in range(3))
+        for causal in (False, True):
+            o, lse = oracle.attention(q, k, v, 0.125, causal, lib=lib)
+            of, lf = oracle.floor_attention(q, k, v, 0.125, causal, fmt, lib=lib)
+            err = np.abs(of - o).max()
+            assert 0.0 < err < 4 * u * np.abs(v).max()
+            assert np.abs(lf - lse).max() < 1e-4
+
+
+FLOOR_PINS = [pin_floor_library_path, pin_floor_q_zero_closed_form,
+              pin_floor_single_key_exact, pin_floor_output_on_grid,
+              pin_floor_within_oracle_rounding]

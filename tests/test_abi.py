@@ -30,7 +30,8 @@ def test_header_declares_the_boundary():
     for n in ("fa_fwd", "fa_fwd_ex", "fa_workspace_bytes", "fa_fwd_host",
               "fa_host_staging_bytes", "fa_get_device_status",
               "fa_set_watchdog_ns", "fa_status_string", "fa_version",
-              "fa_prefill_uses_pairs"):
+              "fa_prefill_uses_pairs", "fa_release_workspaces",
+              "fa_fwd_decode_static"):
         assert n in names, n
 
 
@@ -44,7 +45,7 @@ def test_status_strings_and_version(lib):
     for st in range(6):
         assert fa.fa_status_string(st)
     assert fa.fa_status_string(99) == "unknown status"
-    assert fa.fa_version() == 10100
+    assert fa.fa_version() == 10200
 
 
 def test_pair_selection_without_a_gpu(lib):
@@ -90,6 +91,21 @@ def test_argument_errors_precede_any_cuda_call(lib, kw, want):
     assert _call(lib, **kw) == want
 
 
+@pytest.mark.parametrize("kw,want", [
+    (dict(q=0), 1), (dict(lse=0), 1), (dict(k=24), 1), (dict(B=0), 1),
+    (dict(Skv=0), 1), (dict(scale=0.0), 1), (dict(D=96), 2), (dict(dtype=2), 2),
+])
+def test_static_decode_argument_errors_precede_any_cuda_call(lib, kw, want):
+    """fa_fwd_decode_static checks its arguments as fa_fwd does, before it
+    looks at the device or its scratch."""
+    a = dict(q=16, k=16, v=16, o=16, lse=16, B=1, H=1, Skv=8, D=64, scale=0.125,
+             dtype=1)
+    a.update(kw)
+    assert lib.fa_fwd_decode_static(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"],
+                                    a["H"], a["Skv"], a["D"], ctypes.c_float(a["scale"]),
+                                    a["dtype"], None) == want
+
+
 def test_workspace_and_staging_sizes(lib):
     from attention_forward_gb300 import fa
     assert fa.fa_workspace_bytes(1, 1, 128, 128, 128) == 0   # one key tile: no split
@@ -127,7 +143,8 @@ def test_product_path_does_not_touch_the_oracle():
                 src = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in src and "from oracle" not in src, f
                 assert "liboracle" not in src, f
-    from attention_forward_gb300 import _build
+    from attention_forward_gb300 import _build, fa
     _build.build()
-    data = open(_build.LIB, "rb").read()
-    assert b"oracle_attention_rows" not in data
+    lib = fa.load()
+    for name in ("oracle_attention_rows", "floor_attention_rows", "oracle_probs"):
+        assert not hasattr(lib, name), name

@@ -81,3 +81,59 @@ def test_extreme_scales_through_key_splits(shape, scale, D):
     o, lse = run_kernel(q, k, v, False, scale=scale)
     r = check(q, k, v, o, lse, False, "bf16", scale=scale)
     assert r.passed, str(r)
+
+
+def test_ex2_special_values_on_the_device():
+    """The exponential every kernel's softmax uses (ex2.approx.ftz.f32, run
+    through fa_ex2_approx): 2^-inf = +0 (masked keys), 2^0 = 1 (the row max),
+    exact powers of two, results below the normal range flushed to +0,
+    +inf and NaN propagated ("The FA5090 Optimization Journey", section 2.6,
+    asserts the first two on the device)."""
+    import math
+    x = torch.tensor([-math.inf, 0.0, -0.0, 1.0, -1.0, 8.0, -8.0, 100.0, -126.0,
+                      -127.5, -200.0, math.inf, math.nan], device="cuda")
+    y = fa.fa_ex2_approx(x).cpu()
+    torch.cuda.synchronize()
+    bits = y.view(torch.int32)
+    assert bits[0].item() == 0          # +0, not -0
+    assert y[1].item() == 1.0 and y[2].item() == 1.0
+    assert y[3].item() == 2.0 and y[4].item() == 0.5
+    assert y[5].item() == 256.0 and y[6].item() == 2.0 ** -8
+    assert y[7].item() == 2.0 ** 100
+    assert y[8].item() == 2.0 ** -126
+    assert bits[9].item() == 0 and bits[10].item() == 0   # flushed to +0
+    assert math.isinf(y[11].item()) and y[11].item() > 0
+    assert math.isnan(y[12].item())
+
+
+def test_ex2_accuracy_over_the_softmax_range():
+    """Relative error of 2^x against fp64 over the arguments the softmax
+    sees (x <= 0 after the max is subtracted, and a little above 0 under the
+    lazy-rescale threshold): within 2^-20, far below the 16-bit rounding of
+    P."""
+    import numpy as np
+    g = torch.Generator().manual_seed(7)
+    x = torch.cat([torch.rand(200000, generator=g) * -120.0,
+                   torch.rand(50000, generator=g) * 8.0 - 4.0])
+    y = fa.fa_ex2_approx(x.cuda()).cpu().double().numpy()
+    ref = np.exp2(x.double().numpy())
+    rel = np.abs(y - ref) / ref
+    assert rel.max() <= 2.0 ** -20, rel.max()
+
+
+@pytest.mark.parametrize("kernel", KERNELS, ids=lambda k: k[0])
+def test_special_values_through_the_hot_path(kernel):
+    """Causal rows with exactly one visible key: its score is the row max,
+    so p = 2^0 = 1, every other key is masked to -inf and gives p = 2^-inf
+    = 0, l = 1: the output row is that V row bit for bit, and LSE is the
+    scaled score.  Rows with no visible key (Sq > Skv, bottom-right causal)
+    give O = 0 and LSE = -inf."""
+    _, D, flags = kernel
+    Sq, Skv = 700, 600   # rows 0..99 see no key, row 100 sees key 0 only
+    q, k, v = inputs.make_qkv(1, 3, Sq, Skv, D, "bf16", 61)
+    o, lse = run_kernel(q, k, v, True, flags=flags)
+    o, lse = o.cpu(), lse.cpu()
+    assert torch.all(o[:, :, :100] == 0) and torch.all(torch.isneginf(lse[:, :, :100]))
+    assert torch.equal(o[:, :, 100], v[:, :, 0])
+    s00 = (q[:, :, 100].double() * k[:, :, 0].double()).sum(-1) * D ** -0.5
+    assert (lse[:, :, 100].double() - s00).abs().max().item() < 1e-5

@@ -36,6 +36,66 @@ MUTANTS = {
 }
 
 
+# Planted mistakes in the fp32 floor reference (attend_row_floor and its
+# call): each would make the floor's error larger (or wrong), which would
+# loosen the parity bound.  (site, replacement, occurrence of the site in the
+# file, counting from 0: the floor's copy of a line the fp64 oracle shares)
+FLOOR_MUTANTS = {
+    "floor_scores_rounded_to_16_bits": ("p[j] = scale * dot;",
+                                        "p[j] = round_f32_to_fmt(scale * dot, fmt);", 1),
+    "floor_scale_dropped": ("p[j] = scale * dot;", "p[j] = dot;", 1),
+    "floor_p_rounded_before_normalising": (
+        "p[j] = round_f32_to_fmt(p[j] / l, fmt);",
+        "p[j] = round_f32_to_fmt(p[j], fmt) / l;", 0),
+    "floor_p_not_rounded": ("p[j] = round_f32_to_fmt(p[j] / l, fmt);", "p[j] = p[j] / l;", 0),
+    "floor_l_from_rounded_p": ("l += p[j];", "l += round_f32_to_fmt(p[j], fmt);", 1),
+    "floor_o_not_rounded": ("for (long d = 0; d < D; ++d) o[d] = round_f32_to_fmt(o[d], fmt);",
+                            "", 0),
+    "floor_accumulate_dropped": ("o[d] += p[j] * V[j * D + d];", "o[d] = p[j] * V[j * D + d];", 0),
+    "floor_v_rows_reversed": ("o[d] += p[j] * V[j * D + d];",
+                              "o[d] += p[j] * V[(n - 1 - j) * D + d];", 0),
+    "floor_causal_ignored": ("(const float *)J->v + kvoff, n, D,",
+                             "(const float *)J->v + kvoff, J->Skv, D,", 0),
+    "floor_other_format": ("(float)J->scale, J->fmt,", "(float)J->scale, 1 - J->fmt,", 0),
+    "floor_lse_without_max": ("*lse = m + logf(l);", "*lse = logf(l);", 0),
+}
+
+
+def _compile_mutant(tmp_path, name, at, old, new):
+    src = open(SRC).read()
+    mpath = tmp_path / f"{name}.c"
+    mpath.write_text(src[:at] + new + src[at + len(old):])
+    so = str(tmp_path / f"lib{name}.so")
+    oracle.compile_oracle(str(mpath), so)
+    return oracle.load(so)
+
+
+def _caught_by(lib, pins):
+    caught = []
+    for pin in pins:
+        try:
+            pin(lib)
+        except AssertionError:
+            caught.append(pin.__name__)
+    return caught
+
+
+@pytest.mark.parametrize("name", sorted(FLOOR_MUTANTS))
+def test_floor_mutant_is_caught(tmp_path, name):
+    old, new, nth = FLOOR_MUTANTS[name]
+    src = open(SRC).read()
+    floor_start = src.index("static void attend_row_floor")
+    at = -1
+    for _ in range(nth + 1):
+        at = src.find(old, at + 1)
+        assert at >= 0, name
+    # the site lies in the floor's code (or its call in the row worker)
+    assert at > floor_start, name
+    lib = _compile_mutant(tmp_path, name, at, old, new)
+    caught = _caught_by(lib, oracle_pins.FLOOR_PINS)
+    assert caught, f"no floor pin rejects mutant {name}"
+
+
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_mutant_is_caught(tmp_path, name):
     old, new = MUTANTS[name]

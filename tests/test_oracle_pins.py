@@ -17,6 +17,11 @@ def test_pin(lib, pin):
     pin(lib)
 
 
+@pytest.mark.parametrize("pin", oracle_pins.FLOOR_PINS, ids=lambda f: f.__name__)
+def test_floor_pin(lib, pin):
+    pin(lib)
+
+
 def test_thread_count_does_not_change_results(lib):
     rng = np.random.default_rng(3)
     q, k, v = (rng.standard_normal((2, 3, 33, 16)) for _ in range(3))
@@ -51,29 +56,3 @@ def test_round_fmt_matches_torch_casts(lib, fmt, tdt):
     got = oracle.round_fmt(x, fmt, lib=lib)
     ref = torch.from_numpy(x).to(tdt).float().numpy()
     assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
-
-
-@pytest.mark.parametrize("dtype,fmt,u", [("bf16", oracle.FMT_BF16, 2.0 ** -8),
-                                         ("fp16", oracle.FMT_F16, 2.0 ** -11)])
-def test_floor_error_is_a_rounding_floor(lib, dtype, fmt, u):
-    """The fp32 floor differs from the fp64 oracle by a few units of 16-bit
-    rounding of O (it rounds P and O), and not by more."""
-    from attention_forward_gb300 import inputs
-    q, k, v = inputs.make_qkv(1, 2, 200, 200, 64, dtype, 5)
-    qf, kf, vf = (t.float().numpy() for t in (q, k, v))
-    for causal in (False, True):
-        o, lse = oracle.attention(qf, kf, vf, 0.125, causal, lib=lib)
-        of, lf = oracle.floor_attention(qf, kf, vf, 0.125, causal, fmt, lib=lib)
-        err = np.abs(of - o).max()
-        assert 0.0 < err < 4 * u * np.abs(vf).max()
-        assert np.abs(lf - lse).max() < 1e-4
-
-
-def test_floor_single_key_is_exact(lib):
-    """With one visible key P = 1 exactly, so the floor returns V_0 exactly."""
-    from attention_forward_gb300 import inputs
-    q, k, v = inputs.make_qkv(1, 1, 4, 4, 64, "bf16", 6)
-    qf, kf, vf = (t.float().numpy() for t in (q, k, v))
-    of, _ = oracle.floor_attention(qf, kf, vf, 0.125, True, oracle.FMT_BF16,
-                                   lib=lib)
-    assert np.array_equal(of[0, 0, 0], vf[0, 0, 0])

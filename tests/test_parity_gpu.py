@@ -92,23 +92,42 @@ def test_headline_sampled_rows():
     """B4 H16 S4096 D128 bf16 non-causal at full size, in the launch the bench
     times (fa_fwd, default options); >= 512 sampled rows covering every head."""
     w = inputs.HEADLINE
-    rows = sample_rows(w.B, w.H, w.Sq, per_head=8, extra=256, seed=1)
-    assert rows.size >= 512
+    rows = rows_at_least(w, seed=1)
     _assert(run_and_check(w.B, w.H, w.Sq, w.Skv, w.D, w.dtype, w.causal,
                           w.seed, rows=rows))
+
+
+def rows_at_least(w, n=512, seed=0):
+    """At least n sampled rows of a large workload: tile-edge, first and last
+    rows of every head plus random rows, spread so that every head gets its
+    share."""
+    per_head = max(8, 2 * -(-n // (w.B * w.H)))
+    rows = sample_rows(w.B, w.H, w.Sq, per_head=per_head, extra=256, seed=seed)
+    assert rows.size >= n and np.unique(rows // w.Sq).size == w.B * w.H
+    return rows
 
 
 @pytest.mark.parametrize("w", [inputs.LONG16K, inputs.LONG32K],
                          ids=lambda w: w.name)
 def test_long_causal_sampled_rows(w):
-    rows = sample_rows(w.B, w.H, w.Sq, per_head=24, extra=128, seed=2)
+    """Both long causal workloads at full size, >= 512 sampled rows."""
+    rows = rows_at_least(w, seed=2)
     _assert(run_and_check(w.B, w.H, w.Sq, w.Skv, w.D, w.dtype, w.causal,
                           w.seed, rows=rows))
 
 
-@pytest.mark.parametrize("w", inputs.SWEEP, ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [w for w in inputs.SWEEP if w.Sq <= 2048],
+                         ids=lambda w: w.name)
+def test_sweep_all_rows(w):
+    """The B*S = 16384 sweep up to S = 2048: every output row."""
+    _assert(run_and_check(w.B, w.H, w.Sq, w.Skv, w.D, w.dtype, w.causal, w.seed))
+
+
+@pytest.mark.parametrize("w", [w for w in inputs.SWEEP if w.Sq > 2048],
+                         ids=lambda w: w.name)
 def test_sweep_sampled_rows(w):
-    rows = sample_rows(w.B, w.H, w.Sq, per_head=2, extra=64, seed=3)
+    """The sweep from S = 4096 on: >= 512 sampled rows covering every head."""
+    rows = rows_at_least(w, seed=3)
     _assert(run_and_check(w.B, w.H, w.Sq, w.Skv, w.D, w.dtype, w.causal,
                           w.seed, rows=rows))
 

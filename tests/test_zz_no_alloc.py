@@ -1,12 +1,14 @@
 """fa_fwd_decode_static: the decode pass for callers that cannot allocate
 device memory (its split partials live in the library's static device
-scratch).  Collected last on purpose, so a run that stops at the first
-failure has already run every other test.
+scratch instead of a cudaMalloc'd workspace).  Collected last on purpose, so
+a run that stops at the first failure has already run every other test.
 
-Checked through the C ABI against the existing decode entry point (fa_fwd)
-on two calls in a row with different inputs (the second call reuses the
-scratch the first one left behind), within the gate's tolerances; and a
-shape whose partials exceed the static scratch is rejected up front."""
+Checked through the C ABI against the existing decode entry point (fa_fwd):
+both run the same kernels with the same split on the same inputs, so on two
+calls in a row with different inputs (the second call reuses the scratch the
+first one left behind) the outputs must be equal bit for bit; the static
+path is also gated against the fp64 oracle directly.  A shape whose partials
+exceed the static scratch is rejected up front."""
 import ctypes
 
 import pytest
@@ -50,8 +52,26 @@ def test_two_calls_in_a_row_match_fa_fwd(B, H, Skv, D, dt):
         o_r, l_r = fa.fa_fwd(q, k, v)
         torch.cuda.synchronize()
         assert fa.fa_get_device_status() == fa.FA_OK
+        # the same kernels, split and inputs: identical bits (a partial left
+        # over from the previous call in the shared scratch would show here)
+        assert torch.equal(o_s, o_r) and torch.equal(l_s, l_r), seed
         assert (o_s.float() - o_r.float()).abs().max().item() <= O_TOL[dt]
         assert (l_s - l_r).abs().max().item() <= LSE_TOL
+
+
+def test_static_path_passes_the_oracle_gate():
+    """The static entry point's own output against the fp64 oracle (all rows,
+    the parity gate), after a call on other inputs has filled the scratch."""
+    from parity import check
+    B, H, Skv, D, dt = 4, 8, 3000, 128, "bf16"
+    assert fa.fa_workspace_bytes(B, H, 1, Skv, D) > 0
+    q0, k0, v0 = (t.cuda() for t in inputs.make_qkv(B, H, 1, Skv, D, dt, 40, 3.0))
+    _static_call(q0, k0, v0)
+    q, k, v = inputs.make_qkv(B, H, 1, Skv, D, dt, 41)
+    o, lse = _static_call(q.cuda(), k.cuda(), v.cuda())
+    torch.cuda.synchronize()
+    r = check(q, k, v, o, lse, False, dt)
+    assert r.passed, str(r)
 
 
 def test_too_large_for_the_static_scratch_is_rejected():
