@@ -52,41 +52,53 @@ def _fingerprint() -> str:
     return h.hexdigest()
 
 
-def _compile(src: str) -> tuple[str, str]:
-    obj = os.path.join(OBJ, os.path.splitext(src)[0] + ".o")
-    cmd = [nvcc(), *NVCC_FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+def _compile(src: str, obj_dir: str = OBJ, defines=()) -> tuple[str, str]:
+    obj = os.path.join(obj_dir, os.path.splitext(src)[0] + ".o")
+    cmd = [nvcc(), *NVCC_FLAGS, *[f"-D{d}" for d in defines], "-c",
+           os.path.join(CSRC, src), "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
     return obj, r.stdout + r.stderr
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile and link the library unless an up-to-date build exists."""
-    os.makedirs(OBJ, exist_ok=True)
-    stamp = os.path.join(OBJ, "fingerprint")
-    fp = _fingerprint()
-    if (not force and os.path.exists(LIB) and os.path.exists(stamp)
+def build(force: bool = False, verbose: bool = False, defines=(),
+          variant: str | None = None) -> str:
+    """Compile and link the library unless an up-to-date build exists.
+
+    ``variant`` with ``defines`` (macro names, optionally NAME=VALUE) builds
+    another copy of the same sources with those macros set, into
+    ``_variants/libfa_gb300_<variant>.so``: the alternative arms of paired
+    measurements (bench.py --paired).  The in-tree library is unaffected."""
+    defines = tuple(defines)
+    obj_dir, lib = OBJ, LIB
+    if variant is not None:
+        obj_dir = os.path.join(PKG, "_variants", f"objs_{variant}")
+        lib = os.path.join(PKG, "_variants", f"libfa_gb300_{variant}.so")
+    os.makedirs(obj_dir, exist_ok=True)
+    stamp = os.path.join(obj_dir, "fingerprint")
+    fp = _fingerprint() + " ".join(defines)
+    if (not force and os.path.exists(lib) and os.path.exists(stamp)
             and open(stamp).read() == fp):
-        return LIB
+        return lib
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        results = list(ex.map(_compile, SOURCES))
-    with open(PTXAS_LOG, "w") as f:
+        results = list(ex.map(lambda s: _compile(s, obj_dir, defines), SOURCES))
+    with open(os.path.join(obj_dir, "ptxas.log"), "w") as f:
         for (obj, log), src in zip(results, SOURCES):
             f.write(f"==== {src}\n{log}\n")
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH, "-shared", "--cudart", "shared", "-o", tmp,
            *[o for o, _ in results], f"-L{_cuda_lib_dir()}",
            "-Xlinker", f"-rpath,{_cuda_lib_dir()}"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     with open(stamp, "w") as f:
         f.write(fp)
     if verbose:
-        print(open(PTXAS_LOG).read())
-    return LIB
+        print(open(os.path.join(obj_dir, "ptxas.log")).read())
+    return lib
 
 
 if __name__ == "__main__":

@@ -42,13 +42,21 @@ def lib_path() -> str:
 def load() -> ctypes.CDLL:
     """Load the library; raises if it has not been built."""
     global _lib
-    if _lib is not None:
-        return _lib
-    if not os.path.exists(_LIB_PATH):
+    if _lib is None:
+        _lib = load_path(_LIB_PATH)
+    return _lib
+
+
+def load_path(path: str) -> ctypes.CDLL:
+    """Load a build of the library from ``path`` (the in-tree one, or
+    another build of the same sources, e.g. a variant compared against it
+    in a paired measurement).  Each build loads as its own module, with its
+    own device state."""
+    if not os.path.exists(path):
         raise ImportError(
-            f"{_LIB_PATH} is missing: build it with "
+            f"{path} is missing: build it with "
             "`python -c 'import __graft_entry__ as g; g.build()'`")
-    L = ctypes.CDLL(_LIB_PATH)
+    L = ctypes.CDLL(path)
     vp, ci, cf, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, ci, vp]
     L.fa_fwd.restype = ci
@@ -79,7 +87,6 @@ def load() -> ctypes.CDLL:
     L.fa_ex2_approx.restype = ci
     L.fa_version.argtypes = []
     L.fa_version.restype = ci
-    _lib = L
     return L
 
 
@@ -123,12 +130,13 @@ def _check(status: int, what: str) -> None:
 
 
 def fa_fwd(q, k, v, causal: bool = False, scale: float | None = None,
-           out=None, lse=None, stream=None):
-    """O, LSE = attention(q, k, v) on the library's kernels.  Returns (o, lse)."""
+           out=None, lse=None, stream=None, lib=None):
+    """O, LSE = attention(q, k, v) on the library's kernels.  Returns (o, lse).
+    ``lib``: another loaded build (load_path); default the in-tree one."""
     B, H, Sq, Skv, D = _shape(q, k, v)
     out, lse = _outputs(q, out, lse)
     sc = float(D) ** -0.5 if scale is None else float(scale)
-    st = load().fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+    st = (lib or load()).fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                        lse.data_ptr(), B, H, Sq, Skv, D, sc, int(bool(causal)),
                        _DTYPE[q.dtype], _stream_handle(stream))
     _check(st, "fa_fwd")
@@ -142,7 +150,7 @@ def fa_workspace_bytes(B: int, H: int, Sq: int, Skv: int, D: int,
 
 def fa_fwd_ex(q, k, v, causal: bool = False, scale: float | None = None,
               flags: int = 0, num_splits: int = 0, workspace=None, out=None,
-              lse=None, stream=None):
+              lse=None, stream=None, lib=None):
     """fa_fwd with flags, an explicit decode split count and a caller-owned
     workspace tensor (any dtype, on the device)."""
     B, H, Sq, Skv, D = _shape(q, k, v)
@@ -152,7 +160,7 @@ def fa_fwd_ex(q, k, v, causal: bool = False, scale: float | None = None,
     if workspace is not None:
         ws_ptr = workspace.data_ptr()
         ws_bytes = workspace.numel() * workspace.element_size()
-    st = load().fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+    st = (lib or load()).fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(),
                           out.data_ptr(), lse.data_ptr(), B, H, Sq, Skv, D, sc,
                           int(bool(causal)), _DTYPE[q.dtype], int(flags),
                           int(num_splits), ws_ptr, ws_bytes,

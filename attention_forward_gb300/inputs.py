@@ -146,3 +146,8 @@ SWEEP = _sweep()
 ALL = (PR1, C2, C2_CAUSAL, C2_X4, C2_X4_CAUSAL, HEADLINE, LONG16K, LONG32K,
        DECODE, DECODE_SMALL) + SWEEP
 BY_NAME = {w.name: w for w in ALL}
+# The configured workloads in the order they are listed: the small parity
+# case, the B2 H8 S1024 workloads, the headline, the long causal ones, the
+# B*S = 16384 sweep and decode.
+CONFIGURED = (PR1, C2, C2_CAUSAL, C2_X4, C2_X4_CAUSAL, HEADLINE, LONG16K,
+              LONG32K) + SWEEP + (DECODE,)

@@ -2,6 +2,9 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                     [--impl ours|reference]
+    python bench.py --sweep [--sweep-seconds S]
+    python bench.py --paired [--a-flags F] [--b-flags F] [--b-lib PATH]
+    python bench.py --aa-runs 10
 
 A step is one forward pass (every step of the hot path) over one batch of
 synthetic input already resident in HBM.  The default workload is
@@ -14,6 +17,19 @@ that time.
 
 --impl reference times the CPU oracle (oracle/, fp64 three-step attention) on
 the host cores, on a bounded row sample of the same workload per step.
+
+--sweep prints one line per configured workload (the small parity case, the
+B2 H8 S1024 workloads, the headline, the long causal ones, the B*S = 16384
+sweep and decode), each with its roofline, clocks and a short oracle sample.
+
+--paired is the measurement protocol of "The FA5090 Optimization Journey"
+(section 2.8): two arms of the same workload timed in alternation inside one
+process (order reversed every other alternation), each alternation giving
+one margin t_A / t_B; the line reports the median margin, its spread and the
+AB / BA halves.  Arms differ by fa_fwd_ex flags or by another build of the
+library (_build.build(variant=...)).  --aa-runs N runs the A/A null (both
+arms the same build) in N fresh processes: t_noise = p95 of |margin - 1|,
+and a change is kept only at a margin >= 1 + t_noise.
 """
 from __future__ import annotations
 
@@ -60,6 +76,25 @@ def parse_args(argv=None):
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--ref-seconds", type=float, default=120.0,
                     help="--impl reference: total oracle time over all steps")
+    ap.add_argument("--sweep", action="store_true",
+                    help="one line per configured workload")
+    ap.add_argument("--sweep-only", default="", help="comma-separated workload names")
+    ap.add_argument("--sweep-seconds", type=float, default=0.3,
+                    help="--sweep: GPU time of each workload's timed region")
+    ap.add_argument("--sweep-cpu-seconds", type=float, default=1.5,
+                    help="--sweep: oracle time of each workload's CPU baseline")
+    ap.add_argument("--paired", action="store_true", help="paired A/B of two arms")
+    ap.add_argument("--aa-runs", type=int, default=0,
+                    help="A/A null over this many fresh processes")
+    ap.add_argument("--a-flags", type=lambda x: int(x, 0), default=0)
+    ap.add_argument("--b-flags", type=lambda x: int(x, 0), default=0)
+    ap.add_argument("--a-lib", default="", help="another build of the library for arm A")
+    ap.add_argument("--b-lib", default="", help="another build of the library for arm B")
+    ap.add_argument("--a-tag", default="A")
+    ap.add_argument("--b-tag", default="B")
+    ap.add_argument("--alternations", type=int, default=120)
+    ap.add_argument("--pwarm", type=int, default=25)
+    ap.add_argument("--pmeasure", type=int, default=100)
     return ap.parse_args(argv)
 
 
@@ -144,8 +179,80 @@ def profiled_traffic(kind: str, workload: str):
     return e.get("dram_bytes_per_launch")
 
 
-class ClockSampler:
-    """nvidia-smi clocks / throttle reasons, stamped on arrival."""
+class NvmlClocks:
+    """SM clock, power and clock-event reasons of one GPU, read in-process
+    through NVML (read-only queries, nothing is set) about every half
+    millisecond by a background thread, each sample stamped on arrival.
+    Fast enough for timed regions of a few milliseconds."""
+    # nvmlClocksEventReasons bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+    NVML_CLOCK_SM = 1
+
+    def __init__(self, pci_bus_id: str, period_s: float = 0.0005):
+        import ctypes
+        self.ct = ctypes
+        self.samples = []
+        self.ok = False
+        self.period = period_s
+        self._stop = threading.Event()
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError:
+            return
+        if nv.nvmlInit_v2() != 0:
+            return
+        h = ctypes.c_void_p()
+        if nv.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(), ctypes.byref(h)) != 0:
+            return
+        self.nv, self.h = nv, h
+        mx = ctypes.c_uint(0)
+        self.max_mhz = (float(mx.value) if nv.nvmlDeviceGetMaxClockInfo(
+            h, self.NVML_CLOCK_SM, ctypes.byref(mx)) == 0 else None)
+        self.reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons", None)
+        self.ok = True
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+
+    def _run(self):
+        ct, nv, h = self.ct, self.nv, self.h
+        mhz, mw, rs = ct.c_uint(0), ct.c_uint(0), ct.c_ulonglong(0)
+        while not self._stop.is_set():
+            if nv.nvmlDeviceGetClockInfo(h, self.NVML_CLOCK_SM, ct.byref(mhz)) == 0:
+                w = mw.value / 1e3 if nv.nvmlDeviceGetPowerUsage(h, ct.byref(mw)) == 0 else None
+                r = rs.value if (self.reasons_fn and self.reasons_fn(h, ct.byref(rs)) == 0) else 0
+                self.samples.append((time.time(), float(mhz.value), w, r))
+            time.sleep(self.period)
+
+    def stop(self):
+        self._stop.set()
+        if self.ok:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0: float, t1: float):
+        inside = [x for x in self.samples if t0 <= x[0] <= t1]
+        out = {"sm_mhz": None, "sm_max_mhz": self.max_mhz if self.ok else None,
+               "reasons": [], "samples": len(inside), "source": "nvml, in-process"}
+        if not inside:
+            out["note"] = "no clock sample inside the timed region"
+            return out
+        reasons = set()
+        for _, _, _, r in inside:
+            reasons |= {n for bit, n in self.REASONS.items() if r & bit}
+        pw = [x[2] for x in inside if x[2] is not None]
+        out.update(sm_mhz=statistics.median(x[1] for x in inside),
+                   sm_mhz_min=min(x[1] for x in inside),
+                   power_w_median=statistics.median(pw) if pw else None,
+                   reasons=sorted(reasons))
+        if len(inside) < 3:
+            out["note"] = "fewer than 3 samples inside the timed region"
+        return out
+
+
+class SmiClocks:
+    """Fallback without NVML: nvidia-smi clocks / throttle reasons every
+    20 ms, stamped on arrival; only samples inside the timed region count."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -177,14 +284,8 @@ class ClockSampler:
 
     def summary(self, t0: float, t1: float):
         inside = [s for t, s in self.samples if t0 <= t <= t1]
-        note = "inside timed region"
-        if not inside and self.samples:
-            near = sorted(self.samples, key=lambda ts: min(abs(ts[0] - t0), abs(ts[0] - t1)))
-            inside = [s for _, s in near[:3]]
-            note = "nearest samples (timed region shorter than the sampling period)"
-        if not inside:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
-                    "note": "nvidia-smi unavailable"}
+        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": len(inside),
+               "source": "nvidia-smi -lms 20"}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = set()
         mhz, mx, pw = [], [], []
@@ -198,10 +299,23 @@ class ClockSampler:
             for n, v in zip(names, s[4:8]):
                 if v.strip().lower() == "active":
                     reasons.add(n)
-        return {"sm_mhz": statistics.median(mhz) if mhz else None,
-                "sm_max_mhz": max(mx) if mx else None,
-                "power_w_median": statistics.median(pw) if pw else None,
-                "reasons": sorted(reasons), "samples": len(inside), "note": note}
+        if not mhz:
+            out["note"] = "no clock sample inside the timed region"
+            return out
+        out.update(sm_mhz=statistics.median(mhz), sm_max_mhz=max(mx),
+                   power_w_median=statistics.median(pw) if pw else None,
+                   reasons=sorted(reasons))
+        if len(mhz) < 3:
+            out["note"] = "fewer than 3 samples inside the timed region"
+        return out
+
+
+def clock_sampler(device):
+    """NVML in-process sampler, else nvidia-smi."""
+    c = NvmlClocks(gpu_id_for_smi(device))
+    if c.ok:
+        return c
+    return SmiClocks(gpu_id_for_smi(device))
 
 
 def gpu_id_for_smi(device) -> str:
@@ -335,6 +449,136 @@ def workload_config(w, n_gpus):
             "parallelism": f"independent batches x{n_gpus}"}
 
 
+def launches_per_step(fa, w) -> int:
+    """Kernel launches of one fa_fwd call: the fused kernel, plus the
+    combine kernel when the keys are split (decode, and prefill whose items
+    do not fill the SMs)."""
+    return 2 if fa.fa_workspace_bytes(w.B, w.H, w.Sq, w.Skv, w.D) > 0 else 1
+
+
+def algorithmic_bytes(w) -> int:
+    """Q, K, V read once, O and LSE written once."""
+    return (w.B * w.H * (w.Sq + 2 * w.Skv) * w.D * 2 + w.B * w.H * w.Sq * w.D * 2
+            + w.B * w.H * w.Sq * 4)
+
+
+def roofline(fa, w, launch_s, kflags):
+    """The roofline object of the step's dominant kernel."""
+    peaks, peak_src = load_peaks()
+    if w.Sq == 1:
+        achieved = algorithmic_bytes(w) / launch_s / 1e9
+        peak = float(peaks["hbm_gbs"])
+        return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": profiled_traffic("decode", w.name),
+                "peak_source": f"{peak_src} hbm_gbs",
+                "kernel": "fa_decode_kernel + fa_decode_combine_kernel (one step)"}
+    achieved = w.flops() / launch_s / 1e12
+    peak = float(peaks["bf16_tflops"])
+    pairs = fa.fa_prefill_uses_pairs(w.B, w.H, w.Sq, w.Skv, w.D, w.causal, kflags)
+    kern = "fa_prefill_pair_kernel (two-CTA clusters)" if pairs else "fa_prefill_kernel"
+    if launches_per_step(fa, w) > 1 and not pairs:
+        kern += " with split keys + fa_decode_combine_kernel (one step)"
+    return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak,
+            "traffic": profiled_traffic("prefill_pair" if pairs else "prefill_single", w.name),
+            "peak_source": f"{peak_src} bf16_tflops (burst; dense fp16 has the same rate)",
+            "kernel": kern}
+
+
+class Problem:
+    """One workload's device inputs and outputs, and its step (one fa_fwd or
+    fa_fwd_ex call on `stream`)."""
+
+    def __init__(self, w, device, stream, seed=None, kflags=0, lib=None):
+        from attention_forward_gb300 import fa
+        self.fa, self.w, self.device, self.stream = fa, w, device, stream
+        q, k, v = inputs.make_qkv(w.B, w.H, w.Sq, w.Skv, w.D, w.dtype,
+                                  w.seed if seed is None else seed, w.qk_mult)
+        self.host = (q, k, v)
+        self.dq, self.dk, self.dv = (t.to(device) for t in (q, k, v))
+        self.o = torch.empty_like(self.dq)
+        self.lse = torch.empty((w.B, w.H, w.Sq), dtype=torch.float32, device=device)
+        self.kflags, self.lib = kflags, lib
+
+    def step(self, kflags=None, lib=None):
+        kflags = self.kflags if kflags is None else kflags
+        lib = lib or self.lib
+        if kflags or lib is not None:
+            self.fa.fa_fwd_ex(self.dq, self.dk, self.dv, causal=self.w.causal, flags=kflags,
+                              out=self.o, lse=self.lse, stream=self.stream, lib=lib)
+        else:
+            self.fa.fa_fwd(self.dq, self.dk, self.dv, causal=self.w.causal, out=self.o,
+                           lse=self.lse, stream=self.stream)
+
+
+def timed_steps(prob, K, warmup, world=1, sampler=None):
+    """W untimed steps, then exactly K steps bracketed by a barrier and a
+    synchronize on both sides, with CUDA events on the launching stream
+    around the whole region and around every step.  Returns (seconds of the
+    region, sorted per-step ms, clock summary)."""
+    fa, device, stream = prob.fa, prob.device, prob.stream
+    for _ in range(max(3, warmup)):
+        prob.step()
+    torch.cuda.synchronize(device)
+    if fa.fa_get_device_status() != fa.FA_OK:
+        raise RuntimeError("kernel watchdog fired during warm-up")
+    own = sampler is None
+    if own:
+        sampler = clock_sampler(device)
+        time.sleep(0.05)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world, device)
+    torch.cuda.synchronize(device)
+    wall0 = time.time()
+    t_start.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        prob.step()
+        ev[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(device)
+    wall1 = time.time()
+    barrier(world, device)
+    clocks = sampler.summary(wall0, wall1)
+    if own:
+        sampler.stop()
+    if fa.fa_get_device_status() != fa.FA_OK:
+        raise RuntimeError("kernel watchdog fired in the timed region")
+    total_s = t_start.elapsed_time(t_end) / 1e3
+    launch_ms = sorted(a.elapsed_time(b) for a, b in ev)
+    return total_s, launch_ms, clocks
+
+
+def result_line(prob, K, warmup, world, total_max, launch_ms, clocks):
+    """The JSON line of one timed run (without e2e and the CPU baseline)."""
+    fa, w = prob.fa, prob.w
+    launch_s = statistics.mean(launch_ms) / 1e3
+    pct = lambda f: launch_ms[min(K - 1, int(f * K))]
+    roof = roofline(fa, w, launch_s, prob.kflags)
+    n_in = 3 * prob.dq.numel() * 2 if w.Sq == w.Skv else (prob.dq.numel() + 2 * prob.dk.numel()) * 2
+    return {
+        "metric": METRIC, "value": job_throughput(w.flops(), K, world, total_max),
+        "unit": UNIT, "n_gpus": world, "steps": K, "warmup": warmup,
+        "ms_per_step": total_max / K * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic (seeded N(0,1), per-rank batches)",
+        "config": dict(workload_config(w, world),
+                       l2=f"inputs {n_in / 2**20:.0f} MiB "
+                          f"{'>' if n_in > L2_BYTES else '<='} L2 129 MiB; no flush"),
+        "roofline": roof,
+        "gpu_launches": K * launches_per_step(fa, w),
+        "step_ms": {"mean": launch_s * 1e3, "median": statistics.median(launch_ms),
+                    "p10": pct(0.10), "p90": pct(0.90), "source": "CUDA events around each step"},
+        "clocks": clocks,
+    }
+
+
+def kernel_flags(fa, name):
+    return {"auto": 0, "single": fa.FA_FLAG_SINGLE_CTA, "pair": fa.FA_FLAG_PAIR}[name]
+
+
 def bench_ours(args, w):
     from attention_forward_gb300 import fa
     rank, world, local = dist_env()
@@ -345,118 +589,177 @@ def bench_ours(args, w):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     fa.load()
-
-    q, k, v = inputs.make_qkv(w.B, w.H, w.Sq, w.Skv, w.D, w.dtype,
-                              shard_seed(w.seed, rank), w.qk_mult)
-    dq, dk, dv = (t.to(device) for t in (q, k, v))
-    o = torch.empty_like(dq)
-    lse = torch.empty((w.B, w.H, w.Sq), dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
+    prob = Problem(w, device, stream, seed=shard_seed(w.seed, rank),
+                   kflags=kernel_flags(fa, args.prefill_kernel))
+    K = args.steps
+    total_s, launch_ms, clocks = timed_steps(prob, K, args.warmup, world)
+    total_max = max_over_ranks(total_s, world, device)
+    line = result_line(prob, K, args.warmup, world, total_max, launch_ms, clocks)
     decode = w.Sq == 1
 
-    kflags = {"auto": 0, "single": fa.FA_FLAG_SINGLE_CTA, "pair": fa.FA_FLAG_PAIR}[args.prefill_kernel]
-
-    def step():
-        if kflags:
-            fa.fa_fwd_ex(dq, dk, dv, causal=w.causal, flags=kflags, out=o, lse=lse, stream=stream)
-        else:
-            fa.fa_fwd(dq, dk, dv, causal=w.causal, out=o, lse=lse, stream=stream)
-
-    launches_per_step = 1
-    if decode:
-        launches_per_step = 2 if fa.fa_workspace_bytes(w.B, w.H, 1, w.Skv, w.D) > 0 else 1
-
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize(device)
-    if fa.fa_get_device_status() != fa.FA_OK:
-        raise RuntimeError("kernel watchdog fired during warm-up")
-
-    sampler = ClockSampler(gpu_id_for_smi(device))
-    time.sleep(0.3)
-    K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(K)]
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world, device)
-    torch.cuda.synchronize(device)
-    wall0 = time.time()
-    t_start.record(stream)
-    for i in range(K):
-        ev[i][0].record(stream)
-        step()
-        ev[i][1].record(stream)
-    t_end.record(stream)
-    torch.cuda.synchronize(device)
-    wall1 = time.time()
-    barrier(world, device)
-    sampler.stop()
-    if fa.fa_get_device_status() != fa.FA_OK:
-        raise RuntimeError("kernel watchdog fired in the timed region")
-
-    total_s = t_start.elapsed_time(t_end) / 1e3
-    launch_ms = sorted(a.elapsed_time(b) for a, b in ev)
-    launch_s = statistics.mean(launch_ms) / 1e3
-    pct = lambda f: launch_ms[min(K - 1, int(f * K))]
-    total_max = max_over_ranks(total_s, world, device)
-    flops_step = w.flops()
-    value = job_throughput(flops_step, K, world, total_max)
-
-    peaks, peak_src = load_peaks()
-    if decode:
-        # algorithmic bytes: read Q, K, V once, write O and LSE
-        nbytes = (w.B * w.H * (w.Sq + 2 * w.Skv) * w.D * 2 + w.B * w.H * w.Sq * w.D * 2
-                  + w.B * w.H * w.Sq * 4)
-        achieved = nbytes / launch_s / 1e9
-        peak = float(peaks["hbm_gbs"])
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": profiled_traffic("decode", w.name),
-                "peak_source": f"{peak_src} hbm_gbs",
-                "kernel": "fa_decode_kernel + fa_decode_combine_kernel (one step)"}
-    else:
-        achieved = flops_step / launch_s / 1e12
-        peak = float(peaks["bf16_tflops"])
-        pairs = fa.fa_prefill_uses_pairs(w.B, w.H, w.Sq, w.Skv, w.D, w.causal, kflags)
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak,
-                "traffic": profiled_traffic("prefill_pair" if pairs else "prefill_single", w.name),
-                "peak_source": f"{peak_src} bf16_tflops (burst; dense fp16 has the same rate)",
-                "kernel": ("fa_prefill_pair_kernel (two-CTA clusters)" if pairs
-                           else "fa_prefill_kernel")}
-
-    line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": total_max / K * 1e3,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": w.dtype, "data": "synthetic (seeded N(0,1), per-rank batches)",
-        "config": dict(workload_config(w, world),
-                       l2=f"inputs {3 * dq.numel() * 2 / 2**20:.0f} MiB "
-                          f"{'>' if 3 * dq.numel() * 2 > L2_BYTES else '<='} L2 129 MiB; no flush"),
-        "roofline": roof,
-        "gpu_launches": K * launches_per_step,
-        "step_ms": {"mean": launch_s * 1e3, "median": statistics.median(launch_ms),
-                    "p10": pct(0.10), "p90": pct(0.90), "source": "CUDA events around each step"},
-        "clocks": sampler.summary(wall0, wall1),
-    }
-
     if not args.no_e2e:
-        line["e2e"] = e2e(w, q, k, v, device, stream, min(K, 40))
+        line["e2e"] = e2e(w, *prob.host, device, stream, min(K, 40))
     if rank == 0 and world == 1 and not args.no_gemm_ceiling:
         g = gemm_ceiling(device)
         line["gemm_ceiling_tflops_same_run"] = g
-        line["frac_of_same_run_gemm"] = roof["achieved"] / g if not decode else None
+        line["frac_of_same_run_gemm"] = line["roofline"]["achieved"] / g if not decode else None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        r, cores, sample, dt = oracle_rate(w, args.cpu_seconds)
-        r1, _, sample1, dt1 = oracle_rate(w, args.cpu_seconds / 2, nthreads=1)
-        line["cpu_baseline"] = {"value": r, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                "sample": sample, "seconds": dt,
-                                "one_core": {"value": r1, "unit": UNIT, "sample": sample1,
-                                             "seconds": dt1}}
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+    return 0
+
+
+def cpu_baseline(w, seconds, one_core=True):
+    r, cores, sample, dt = oracle_rate(w, seconds)
+    out = {"value": r, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
+           "seconds": dt}
+    if one_core:
+        r1, _, sample1, dt1 = oracle_rate(w, seconds / 2, nthreads=1)
+        out["one_core"] = {"value": r1, "unit": UNIT, "sample": sample1, "seconds": dt1}
+    return out
+
+
+def bench_sweep(args):
+    """One JSON line per configured workload on this GPU: as many steps as
+    fill about --sweep-seconds of GPU time (at least 20), the same timing,
+    clock sampling and roofline as the default run, and a short oracle
+    sample on the host cores."""
+    from attention_forward_gb300 import fa
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    fa.load()
+    stream = torch.cuda.current_stream(device)
+    gemm = None if args.no_gemm_ceiling else gemm_ceiling(device)
+    names = args.sweep_only.split(",") if args.sweep_only else None
+    for w in inputs.CONFIGURED:
+        if names and w.name not in names:
+            continue
+        prob = Problem(w, device, stream, kflags=kernel_flags(fa, args.prefill_kernel))
+        # size the run: a few probe steps first
+        for _ in range(3):
+            prob.step()
+        torch.cuda.synchronize(device)
+        t0 = time.perf_counter()
+        for _ in range(5):
+            prob.step()
+        torch.cuda.synchronize(device)
+        per = (time.perf_counter() - t0) / 5
+        K = int(min(5000, max(20, args.sweep_seconds / max(per, 1e-6))))
+        total_s, launch_ms, clocks = timed_steps(prob, K, args.warmup, 1)
+        line = result_line(prob, K, args.warmup, 1, total_s, launch_ms, clocks)
+        if gemm is not None:
+            line["gemm_ceiling_tflops_same_run"] = gemm
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(w, args.sweep_cpu_seconds, one_core=False)
+        print(json.dumps(line), flush=True)
+        del prob
+        torch.cuda.empty_cache()
+    return 0
+
+
+def paired_margins(prob, arms, alternations, pwarm, pmeasure):
+    """The FA5090 paired protocol: per alternation, each arm runs pwarm
+    untimed then pmeasure timed launches (CUDA events per launch) and gives
+    its median; the order is AB on even and BA on odd alternations.
+    Returns the per-alternation (median A ms, median B ms, order)."""
+    out = []
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(pmeasure)]
+    for i in range(alternations):
+        order = (0, 1) if i % 2 == 0 else (1, 0)
+        med = [0.0, 0.0]
+        for a in order:
+            kflags, lib = arms[a]
+            for _ in range(pwarm):
+                prob.step(kflags, lib)
+            for e0, e1 in evs:
+                e0.record(prob.stream)
+                prob.step(kflags, lib)
+                e1.record(prob.stream)
+            torch.cuda.synchronize(prob.device)
+            med[a] = statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
+        out.append((med[0], med[1], "AB" if order == (0, 1) else "BA"))
+    return out
+
+
+def bench_paired(args, w):
+    """Paired, interleaved A/B of two arms on one workload (see the module
+    docstring); prints one JSON line."""
+    from attention_forward_gb300 import fa
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    fa.load()
+    stream = torch.cuda.current_stream(device)
+    libs = [fa.load_path(p) if p else None for p in (args.a_lib, args.b_lib)]
+    arms = [(args.a_flags, libs[0]), (args.b_flags, libs[1])]
+    prob = Problem(w, device, stream)
+    # both arms must compute the same attention: compare their outputs
+    outs = []
+    for kflags, lib in arms:
+        prob.step(kflags, lib)
+        torch.cuda.synchronize(device)
+        outs.append((prob.o.clone(), prob.lse.clone()))
+    bitwise = bool(torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1]))
+    sampler = clock_sampler(device)
+    time.sleep(0.05)
+    wall0 = time.time()
+    res = paired_margins(prob, arms, args.alternations, args.pwarm, args.pmeasure)
+    wall1 = time.time()
+    clocks = sampler.summary(wall0, wall1)
+    sampler.stop()
+    if fa.fa_get_device_status() != fa.FA_OK:
+        raise RuntimeError("kernel watchdog fired in a paired run")
+    m = np.array([a / b for a, b, _ in res])
+    half = lambda o: float(np.median([a / b for a, b, oo in res if oo == o]))
+    line = {
+        "mode": "paired", "workload": w.name,
+        "a": {"flags": args.a_flags, "lib": args.a_lib or "in-tree", "tag": args.a_tag},
+        "b": {"flags": args.b_flags, "lib": args.b_lib or "in-tree", "tag": args.b_tag},
+        "margin": float(np.median(m)),
+        "margin_gmean": float(np.exp(np.mean(np.log(m)))),
+        "paired_lo": float(np.percentile(m, 10)), "paired_hi": float(np.percentile(m, 90)),
+        "ab_half": half("AB"), "ba_half": half("BA"),
+        "b_wins": int((m > 1).sum()), "alternations": len(res),
+        "t_a_ms": float(np.median([a for a, _, _ in res])),
+        "t_b_ms": float(np.median([b for _, b, _ in res])),
+        "protocol": f"{args.alternations} alternations x ({args.pwarm} warm-up + "
+                    f"{args.pmeasure} timed launches per arm), order AB/BA alternating; "
+                    "margin = median_A / median_B per alternation (> 1: B faster)",
+        "outputs_bitwise_equal": bitwise, "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def bench_aa(args, w):
+    """The A/A null: the paired protocol with both arms the same build, in
+    --aa-runs fresh processes; t_noise = p95 of |margin - 1|."""
+    margins, lines = [], []
+    for _ in range(args.aa_runs):
+        cmd = [sys.executable, os.path.abspath(__file__), "--paired", "--workload", w.name,
+               "--alternations", str(args.alternations), "--pwarm", str(args.pwarm),
+               "--pmeasure", str(args.pmeasure), "--a-tag", "A", "--b-tag", "A'"]
+        r = subprocess.run(cmd, capture_output=True, text=True, timeout=1800)
+        if r.returncode != 0:
+            raise RuntimeError(r.stderr[-2000:])
+        d = json.loads([x for x in r.stdout.splitlines() if x.strip()][-1])
+        margins.append(d["margin"])
+        lines.append({k: d[k] for k in ("margin", "ab_half", "ba_half", "b_wins",
+                                        "t_a_ms", "t_b_ms")} | {"sm_mhz": d["clocks"]["sm_mhz"]})
+    dev = np.abs(np.array(margins) - 1.0)
+    t_noise = float(np.percentile(dev, 95))
+    print(json.dumps({"mode": "aa_null", "workload": w.name, "runs": len(margins),
+                      "margins": margins, "t_noise": t_noise,
+                      "t_noise_max": float(dev.max()), "t_keep": 1.0 + t_noise,
+                      "protocol": f"{args.alternations} alternations x ({args.pwarm} + "
+                                  f"{args.pmeasure} launches per arm), each run a fresh "
+                                  "process, both arms the in-tree build",
+                      "per_run": lines}), flush=True)
     return 0
 
 
@@ -505,6 +808,12 @@ def main(argv=None):
     w = inputs.BY_NAME[args.workload]
     if args.impl == "reference":
         return bench_reference(args, w)
+    if args.sweep:
+        return bench_sweep(args)
+    if args.aa_runs:
+        return bench_aa(args, w)
+    if args.paired:
+        return bench_paired(args, w)
     return bench_ours(args, w)
 
 
