@@ -695,7 +695,8 @@ def bench_paired(args, w):
     torch.cuda.set_device(device)
     fa.load()
     stream = torch.cuda.current_stream(device)
-    libs = [fa.load_path(p) if p else None for p in (args.a_lib, args.b_lib)]
+    # both arms call fa_fwd_ex (the in-tree build unless another is given)
+    libs = [fa.load_path(p) if p else fa.load() for p in (args.a_lib, args.b_lib)]
     arms = [(args.a_flags, libs[0]), (args.b_flags, libs[1])]
     prob = Problem(w, device, stream)
     # both arms must compute the same attention: compare their outputs
