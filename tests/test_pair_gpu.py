@@ -161,3 +161,21 @@ def test_pair_scheduler_slots_wrap_around():
             torch.cuda.synchronize()
             assert torch.equal(o, ref) and torch.equal(lse, lref), i
     assert fa.fa_get_device_status() == fa.FA_OK
+
+
+@pytest.mark.parametrize("case", [(4, 16, 4096, 4096, False), (2, 32, 2048, 2048, True),
+                                  (8, 16, 1000, 1000, True)],
+                         ids=lambda c: "x".join(map(str, c)))
+def test_pair_many_items_per_cta_match_single_cta_bitwise(case):
+    """Many items per pair (the item ring wraps dozens of times) give the
+    same bits as the single-CTA kernel, which computes every element in the
+    same order.  The pair kernel frees an item-ring slot with a relaxed
+    cluster arrive, ordered after the read of the slot only by its control
+    dependency on the value read; a slot overwritten before a taker read it
+    would hand that taker another item and change the output here."""
+    B, H, S, _, causal = case
+    q, k, v = inputs.make_qkv(B, H, S, S, 128, "bf16", 71)
+    ref = run_kernel(q, k, v, causal, flags=fa.FA_FLAG_SINGLE_CTA)
+    for _ in range(3):
+        o, lse = run_kernel(q, k, v, causal, flags=fa.FA_FLAG_PAIR)
+        assert torch.equal(o, ref[0]) and torch.equal(lse, ref[1])
