@@ -23,10 +23,10 @@ int prefill_smem_bytes_d128();
 int prefill_smem_bytes_d64();
 cudaError_t prefill_num_regs_d128(bool bf16, int* regs);
 cudaError_t prefill_num_regs_d64(bool bf16, int* regs);
-cudaError_t launch_prefill_d128(bool, const CUtensorMap&, const CUtensorMap&,
+cudaError_t launch_prefill_d128(bool, bool, const CUtensorMap&, const CUtensorMap&,
                                 const CUtensorMap&, const CUtensorMap&,
                                 const PrefillParams&, int, cudaStream_t);
-cudaError_t launch_prefill_d64(bool, const CUtensorMap&, const CUtensorMap&,
+cudaError_t launch_prefill_d64(bool, bool, const CUtensorMap&, const CUtensorMap&,
                                const CUtensorMap&, const CUtensorMap&,
                                const PrefillParams&, int, cudaStream_t);
 
@@ -37,12 +37,12 @@ cudaError_t prefill_num_regs(int D, bool bf16, int* regs) {
   return D == 128 ? prefill_num_regs_d128(bf16, regs)
                   : prefill_num_regs_d64(bf16, regs);
 }
-cudaError_t launch_prefill(int D, bool bf16, const CUtensorMap& q,
+cudaError_t launch_prefill(int D, bool bf16, bool corr, const CUtensorMap& q,
                            const CUtensorMap& k, const CUtensorMap& v,
                            const CUtensorMap& o, const PrefillParams& p,
                            int grid, cudaStream_t stream) {
-  return D == 128 ? launch_prefill_d128(bf16, q, k, v, o, p, grid, stream)
-                  : launch_prefill_d64(bf16, q, k, v, o, p, grid, stream);
+  return D == 128 ? launch_prefill_d128(bf16, corr, q, k, v, o, p, grid, stream)
+                  : launch_prefill_d64(bf16, corr, q, k, v, o, p, grid, stream);
 }
 
 }  // namespace fa
@@ -313,7 +313,8 @@ fa_status_t run_prefill_pair(DeviceState& d, const void* q, const void* k, const
   p.n_items = static_cast<int>(n_items);
   p.sched = sched_slot(d, captured);
   const int n_pairs = static_cast<int>(std::min<long long>(n_items, d.pair_slots[ti]));
-  if (fa::launch_prefill_pair(bf16, tq, tk, tv, to, p, n_pairs, stream) != cudaSuccess)
+  if (fa::launch_prefill_pair(bf16, (flags & FA_FLAG_CORRECTION_WG) != 0, tq, tk, tv, to, p,
+                              n_pairs, stream) != cudaSuccess)
     return FA_ERR_CUDA;
   return FA_OK;
 }
@@ -392,7 +393,8 @@ fa_status_t run_prefill(DeviceState& d, const void* q, const void* k, const void
   p.sched = sched_slot(d, captured);
   // persistent: one CTA per SM (the kernel's shared memory allows no second)
   const int grid = static_cast<int>(std::min<long long>(n_items, d.sm_count > 0 ? d.sm_count : 1));
-  if (fa::launch_prefill(D, bf16, tq, tk, tv, to, p, grid, stream) != cudaSuccess)
+  if (fa::launch_prefill(D, bf16, (flags & FA_FLAG_CORRECTION_WG) != 0, tq, tk, tv, to, p,
+                         grid, stream) != cudaSuccess)
     return FA_ERR_CUDA;
   if (n_splits > 1) {
     // merge the key ranges of every (head, query row): the decode combine

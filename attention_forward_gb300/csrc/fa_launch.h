@@ -11,7 +11,8 @@ namespace fa {
 int prefill_smem_bytes(int D);
 // Registers per thread the compiled prefill kernel was built with.
 cudaError_t prefill_num_regs(int D, bool bf16, int* regs);
-cudaError_t launch_prefill(int D, bool bf16, const CUtensorMap& q,
+// corr: the correction-warpgroup form (ignored with split keys)
+cudaError_t launch_prefill(int D, bool bf16, bool corr, const CUtensorMap& q,
                            const CUtensorMap& k, const CUtensorMap& v,
                            const CUtensorMap& o, const PrefillParams& p,
                            int grid, cudaStream_t stream);
@@ -20,9 +21,10 @@ cudaError_t launch_prefill(int D, bool bf16, const CUtensorMap& q,
 // number of two-CTA clusters that fit on the device, and the launch.
 cudaError_t prefill_pair_num_regs(bool bf16, int* regs);
 cudaError_t prefill_pair_max_pairs(bool bf16, int* n);
-cudaError_t launch_prefill_pair(bool bf16, const CUtensorMap& q, const CUtensorMap& k,
-                                const CUtensorMap& v, const CUtensorMap& o,
-                                const PrefillParams& p, int n_pairs, cudaStream_t stream);
+cudaError_t launch_prefill_pair(bool bf16, bool corr, const CUtensorMap& q,
+                                const CUtensorMap& k, const CUtensorMap& v,
+                                const CUtensorMap& o, const PrefillParams& p, int n_pairs,
+                                cudaStream_t stream);
 
 int decode_smem_bytes(int D);
 cudaError_t launch_decode(int D, bool bf16, const DecodeParams& p, int grid,

@@ -102,10 +102,14 @@ struct PrefillLayout {
   static constexpr int kOffItems = kOffInvL + kStages * kBM * 4;
   static constexpr int kOffTmemSlot = kOffItems + kItemRing * 4;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
-  static constexpr int kMiscBytes = kOffAbort + 4 - kOffMisc;
+  // [2][4] correction requests (the correction-warpgroup form): the softmax
+  // warp of stage s and TMEM lane quarter q -> the epilogue warp of quarter q
+  static constexpr int kOffCorrBars = kOffAbort + 4;
+  static constexpr int kMiscBytes = kOffCorrBars + 8 * 8 - kOffMisc;
   static constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;  // + align
   static constexpr int kTmemCols = 512;
   static constexpr int kTmemO = 256;  // O_s at column 256 + s*D
+  static_assert(kOffCorrBars % 8 == 0, "mbarrier alignment");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
@@ -126,9 +130,21 @@ struct ItemT<true> {
 // more, the others give theirs back.  The sum over the 512 threads equals
 // 512 * 128, the registers the CTA is launched with; the host checks the
 // compiled register count before the first launch.
+// CTA-pair kernel: 192 for each softmax warpgroup, 64 for the others.
 constexpr int kRegsSoftmax = 192;
 constexpr int kRegsOther = 64;
 static_assert(2 * 128 * kRegsSoftmax + 2 * 128 * kRegsOther == kThreads * 128,
+              "register split must equal the launch allocation");
+// Single-CTA kernel: 176 for each softmax warpgroup, 72 for the epilogue
+// warpgroup and 88 for the MMA / producer warpgroup.  With 64 for both of
+// the latter, ptxas spilled in them (4 B stored, 68 B loaded); this split
+// compiles without spills and measured 1.4 % faster on causal S4096 and
+// 0.7 % on D = 64 (paired, interleaved runs).
+constexpr int kRegsSoftmaxSingle = 176;
+constexpr int kRegsEpilogueSingle = 72;
+constexpr int kRegsControlSingle = 88;
+static_assert(128 * (2 * kRegsSoftmaxSingle + kRegsEpilogueSingle + kRegsControlSingle) ==
+                  kThreads * 128,
               "register split must equal the launch allocation");
 
 struct Ctl {
@@ -292,9 +308,11 @@ __device__ __forceinline__ int take_item(const volatile int* ring, uint32_t full
 // kVoteFirst places the warp's vote on that rescale before the exponentials
 // rather than after them: the arithmetic is the same, only the instruction
 // schedule differs (measured faster for the single-CTA kernel, slower for
-// the CTA-pair kernel).
-template <int D, bool BF16, bool kVoteFirst = true>
-__device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int key0, int stage_row0,
+// the CTA-pair kernel).  kDefer leaves the rescale to a correction warp: the
+// tile writes each row's alpha to column 64 of S (past P) instead, and
+// returns true when the warp's rows need it (warp-uniform).
+template <int D, bool BF16, bool kVoteFirst = true, bool kDefer = false>
+__device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tO, int key0, int stage_row0,
                                              int row_g, const PrefillParams& p, bool may_rescale,
                                              float& m, float& l) {
   const int off = p.Skv - p.Sq;
@@ -374,7 +392,10 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int key0,
   m = m_new;
   if constexpr (!kVoteFirst)
     rescale = may_rescale && (p.always_rescale || __any_sync(0xffffffffu, alpha != 1.f));
-  if (rescale) {
+  if constexpr (kDefer) {
+    // the row's S values are no longer needed: alpha for the correction warp
+    if (rescale) tmem_st1(tS + 64, __float_as_uint(alpha));
+  } else if (rescale) {
     // the row's S values are no longer needed: all D columns of O in one
     // tensor-memory round trip (each load-and-wait costs ~240 cycles)
     uint32_t v[D / 16][16];
@@ -391,7 +412,39 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int key0,
     }
   }
   tmem_wait_st();
+  return rescale;
 }
+
+// O_s *= alpha for one warp's 32 rows (the correction-warpgroup form), with
+// alpha read from column 64 of S_s where the softmax warp left it: 32
+// columns of O per tensor-memory round trip (the correction warp runs with
+// the smaller register share).  Ends with tcgen05.wait::st.
+template <int D>
+__device__ __forceinline__ void correct_rows(uint32_t tS, uint32_t tO) {
+  uint32_t a = tmem_ld1(tS + 64);
+  tmem_wait_ld();
+  asm volatile("" : "+r"(a)::"memory");
+  const float alpha = __uint_as_float(a);
+#pragma unroll 1
+  for (int cc = 0; cc < D / 32; ++cc) {
+    uint32_t v[2][16];
+    tmem_ld32(tO + cc * 32, v[0], v[1]);
+    tmem_wait_ld();
+    reg_fence16(v[0]);
+    reg_fence16(v[1]);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+      for (int e = 0; e < 16; ++e) v[h][e] = __float_as_uint(__uint_as_float(v[h][e]) * alpha);
+      tmem_st16(tO + cc * 32 + h * 16, v[h]);
+    }
+  }
+  tmem_wait_st();
+}
+
+// Poll interval of a correction warp (it watches its quarter's requests of
+// both stages and its own epilogue barrier).
+constexpr unsigned kSleepCorrNs = 32;
 
 // The epilogue's staging of 32 rows x D columns of O (this warp's TMEM lane
 // quarter at tO): O * inv_l rounded to 16 bits (zeros when the rows saw no
@@ -430,7 +483,13 @@ __device__ __forceinline__ void stage_o_rows(uint32_t tO, bool have_o, float inv
   }
 }
 
-template <int D, bool BF16, bool kSplit>
+// kCorrWG: the correction-warpgroup form.  The softmax warps do not rescale
+// O themselves; a warp whose rows moved their reference max hands the tile to
+// the epilogue warp of its TMEM lane quarter, which rescales O in tensor
+// memory and makes the tile's PV_READY arrival in its place (the dedicated
+// correction warpgroup of the B300 G5 page, V21).  Tiles without a rescale
+// arrive on PV_READY directly, as in the merged form (G5 V25).
+template <int D, bool BF16, bool kSplit, bool kCorrWG = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_prefill_kernel(const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmK,
@@ -452,6 +511,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile uint32_t* abort_flag =
       reinterpret_cast<volatile uint32_t*>(smem + L::kOffAbort);
   auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
+  auto corr_bar = [&](int s, int q) {
+    return sbase + static_cast<uint32_t>(L::kOffCorrBars + 8 * (s * 4 + q));
+  };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -476,6 +538,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(L::KV_FULL + i), 1);
       mbar_init(bar(L::KV_EMPTY + i), 1);
     }
+    if constexpr (kCorrWG)
+      for (int i = 0; i < 8; ++i) mbar_init(corr_bar(i >> 2, i & 3), 1);
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -497,9 +561,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int wg = warp >> 2;
   if (wg < 2) {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmaxSingle));
+  } else if (wg == 2) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsEpilogueSingle));
   } else {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControlSingle));
   }
 
   if (wg < 2) {
@@ -528,10 +594,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < nT; ++j, ++n_s) {
         if (!wait_bar_warp(bar(L::S_FULL + s), n_s & 1, ctl)) { ok = false; break; }
         tc_fence_after();
-        softmax_tile<D, BF16>(tS, tO, (it.t0 + j) * kBN, stage_row0, row_g, p, j > 0, m, l);
+        const bool defer = softmax_tile<D, BF16, true, kCorrWG>(
+            tS, tO, (it.t0 + j) * kBN, stage_row0, row_g, p, j > 0, m, l);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(L::PV_READY + s));
+        // a rescale request goes to this quarter's correction warp, which
+        // arrives on PV_READY_s in this warp's place
+        if (lane == 0) mbar_arrive(kCorrWG && defer ? corr_bar(s, rq) : bar(L::PV_READY + s));
       }
       if (!ok) break;
 
@@ -564,7 +633,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t stage_buf = sOut + static_cast<uint32_t>(rq * L::kOutWarpBytes);
     uint32_t n_t0 = 0, n_t1 = 0;  // tiles of stage s so far (O_READY phase)
     uint32_t n_e0 = 0, n_e1 = 0;  // ML_FULL phases
+    uint32_t n_c[2] = {0u, 0u};   // correction requests served, per stage
     bool ok = true;
+    // The wait for an item's 1/l (the end of its stage): in the
+    // correction-warpgroup form it also serves this quarter's correction
+    // requests of both stages, polling without suspending; bounded by the
+    // watchdog like every other wait.
+    auto epi_wait = [&](uint32_t b, uint32_t par) -> bool {
+      if constexpr (!kCorrWG) {
+        return wait_bar_warp<kSleepEpilogueNs>(b, par, ctl);
+      } else {
+        uint64_t t0 = 0;
+        for (uint32_t n = 1;; ++n) {
+          if (__any_sync(0xffffffffu, mbar_test_wait(b, par))) return true;
+#pragma unroll
+          for (int s2 = 0; s2 < 2; ++s2) {
+            if (__any_sync(0xffffffffu, mbar_test_wait(corr_bar(s2, rq), n_c[s2] & 1))) {
+              tc_fence_after();
+              correct_rows<D>(tmem + t_lane + static_cast<uint32_t>(s2 * kBN),
+                              tmem + t_lane + static_cast<uint32_t>(L::kTmemO + s2 * D));
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar(L::PV_READY + s2));
+              ++n_c[s2];
+              t0 = 0;
+            }
+          }
+          if ((n & 7u) == 0) {
+            if (*ctl.abort) return false;
+            const uint64_t t = globaltimer_ns();
+            if (t0 == 0) {
+              t0 = t;
+            } else if (t - t0 > ctl.timeout) {
+              *ctl.abort = 1u;
+              atomicExch(ctl.status, kStatusTimeout);
+              return false;
+            }
+          }
+          __nanosleep(kSleepCorrNs);
+        }
+      }
+    };
 #pragma unroll 1
     for (uint32_t k = 0; ok; ++k) {
       const int idx = take_item<kSleepEpilogueNs>(item_ring, bar(L::ITEM_FULL),
@@ -581,7 +690,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t& n_t = s == 0 ? n_t0 : n_t1;
           uint32_t& n_e = s == 0 ? n_e0 : n_e1;
           n_t += static_cast<uint32_t>(nT);
-          if (!wait_bar_warp<kSleepEpilogueNs>(bar(L::ML_FULL + s), n_e & 1, ctl)) { ok = false; continue; }
+          if (!epi_wait(bar(L::ML_FULL + s), n_e & 1)) { ok = false; continue; }
           ++n_e;
           inv_l = inv_l_smem[s * kBM + r];
           if (!wait_bar_warp<kSleepEpilogueNs>(bar(L::O_READY + s), (n_t - 1) & 1, ctl)) { ok = false; continue; }

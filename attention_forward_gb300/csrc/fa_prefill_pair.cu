@@ -1,6 +1,6 @@
 // fa_prefill_pair.cu -- instantiations and launcher of the CTA-pair prefill
-// kernel (head dimension 128, fp16 and bf16, whole key range), launched with
-// clusters of two CTAs.
+// kernel (head dimension 128, fp16 and bf16, whole key range; merged or
+// correction-warpgroup form), launched with clusters of two CTAs.
 #include <mutex>
 
 #include "fa_launch.h"
@@ -9,7 +9,7 @@
 namespace fa {
 namespace {
 
-template <bool BF16>
+template <bool BF16, bool kCorr>
 cudaError_t set_attrs() {
   static std::mutex mu;
   static bool done[64] = {};
@@ -19,7 +19,7 @@ cudaError_t set_attrs() {
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(mu);
   if (done[dev]) return cudaSuccess;
-  e = cudaFuncSetAttribute(fa_prefill_pair_kernel<BF16>,
+  e = cudaFuncSetAttribute(fa_prefill_pair_kernel<BF16, kCorr>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, PairLayout::kSmemBytes);
   if (e == cudaSuccess) done[dev] = true;
   return e;
@@ -40,31 +40,39 @@ cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribut
   return cfg;
 }
 
-template <bool BF16>
+template <bool BF16, bool kCorr>
 cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                    const CUtensorMap& o, const PrefillParams& p, int n_pairs,
                    cudaStream_t stream) {
-  cudaError_t e = set_attrs<BF16>();
+  cudaError_t e = set_attrs<BF16, kCorr>();
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   const cudaLaunchConfig_t cfg = pair_config(2 * n_pairs, stream, attr);
-  return cudaLaunchKernelEx(&cfg, fa_prefill_pair_kernel<BF16>, q, k, v, o, p);
+  return cudaLaunchKernelEx(&cfg, fa_prefill_pair_kernel<BF16, kCorr>, q, k, v, o, p);
 }
 
+// Both forms have the same shared memory and threads, so the same number of
+// pairs fits; the merged form is queried.
 template <bool BF16>
 cudaError_t max_pairs(int* n) {
-  cudaError_t e = set_attrs<BF16>();
+  cudaError_t e = set_attrs<BF16, false>();
+  if (e != cudaSuccess) return e;
+  e = set_attrs<BF16, true>();
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   const cudaLaunchConfig_t cfg = pair_config(2, nullptr, attr);
-  return cudaOccupancyMaxActiveClusters(n, fa_prefill_pair_kernel<BF16>, &cfg);
+  return cudaOccupancyMaxActiveClusters(n, fa_prefill_pair_kernel<BF16, false>, &cfg);
 }
 
+// Registers per thread of both forms: their count, or the first that is not
+// 128 (the register split assumes 128).
 template <bool BF16>
 cudaError_t num_regs(int* regs) {
-  cudaFuncAttributes a{};
-  const cudaError_t e = cudaFuncGetAttributes(&a, fa_prefill_pair_kernel<BF16>);
-  if (e == cudaSuccess) *regs = a.numRegs;
+  cudaFuncAttributes a{}, b{};
+  cudaError_t e = cudaFuncGetAttributes(&a, fa_prefill_pair_kernel<BF16, false>);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncGetAttributes(&b, fa_prefill_pair_kernel<BF16, true>);
+  if (e == cudaSuccess) *regs = a.numRegs != 128 ? a.numRegs : b.numRegs;
   return e;
 }
 
@@ -78,11 +86,15 @@ cudaError_t prefill_pair_num_regs(bool bf16, int* regs) {
   return bf16 ? num_regs<true>(regs) : num_regs<false>(regs);
 }
 
-cudaError_t launch_prefill_pair(bool bf16, const CUtensorMap& q, const CUtensorMap& k,
-                                const CUtensorMap& v, const CUtensorMap& o,
-                                const PrefillParams& p, int n_pairs, cudaStream_t stream) {
-  return bf16 ? launch<true>(q, k, v, o, p, n_pairs, stream)
-              : launch<false>(q, k, v, o, p, n_pairs, stream);
+cudaError_t launch_prefill_pair(bool bf16, bool corr, const CUtensorMap& q,
+                                const CUtensorMap& k, const CUtensorMap& v,
+                                const CUtensorMap& o, const PrefillParams& p, int n_pairs,
+                                cudaStream_t stream) {
+  if (corr)
+    return bf16 ? launch<true, true>(q, k, v, o, p, n_pairs, stream)
+                : launch<false, true>(q, k, v, o, p, n_pairs, stream);
+  return bf16 ? launch<true, false>(q, k, v, o, p, n_pairs, stream)
+              : launch<false, false>(q, k, v, o, p, n_pairs, stream);
 }
 
 }  // namespace fa

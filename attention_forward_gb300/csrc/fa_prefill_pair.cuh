@@ -67,10 +67,12 @@ struct PairLayout {
   static constexpr int kOffItems = kOffInvL + kStages * kBM * 4;
   static constexpr int kOffTmemSlot = kOffItems + kItemRing * 4;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
-  static constexpr int kMiscBytes = kOffAbort + 4 - kOffMisc;
+  static constexpr int kOffCorrBars = kOffAbort + 4;  // [2][4] L/B: local requests
+  static constexpr int kMiscBytes = kOffCorrBars + 8 * 8 - kOffMisc;
   static constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;  // + align
   static constexpr int kTmemCols = 512;
   static constexpr int kTmemO = 256;
+  static_assert(kOffCorrBars % 8 == 0, "mbarrier alignment");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
@@ -168,7 +170,11 @@ constexpr unsigned kPairSleepMmaNs = 33;
 constexpr unsigned kPairSleepProducerNs = 65;
 constexpr unsigned kPairSleepEpilogueNs = 257;
 
-template <bool BF16>
+// kCorrWG: the correction-warpgroup form, as in fa_prefill_kernel: a softmax
+// warp whose rows moved their reference max hands the tile to the epilogue
+// warp of its lane quarter (same CTA), which rescales O and makes the tile's
+// PV_READY arrival on the leader in its place.
+template <bool BF16, bool kCorrWG = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ,
                            const __grid_constant__ CUtensorMap tmK,  // box: 64 keys
@@ -191,6 +197,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile uint32_t* abort_flag =
       reinterpret_cast<volatile uint32_t*>(smem + L::kOffAbort);
   auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
+  auto corr_bar = [&](int s, int q) {
+    return sbase + static_cast<uint32_t>(L::kOffCorrBars + 8 * (s * 4 + q));
+  };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -220,6 +229,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(L::KV_FULL + i), 1);
       mbar_init(bar(L::KV_EMPTY + i), 1);
     }
+    if constexpr (kCorrWG)
+      for (int i = 0; i < 8; ++i) mbar_init(corr_bar(i >> 2, i & 3), 1);
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -276,10 +287,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         // this CTA's rows; the pair's stage may reach one tile further than
         // they need (masked)
-        softmax_tile<D, BF16, false>(tS, tO, j * kBN, stage_row0, row_g, p, j > 0, m, l);
+        const bool defer = softmax_tile<D, BF16, false, kCorrWG>(tS, tO, j * kBN, stage_row0,
+                                                                 row_g, p, j > 0, m, l);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster_relaxed(bar_l(L::PV_READY + s));
+        if (lane == 0) {
+          if (kCorrWG && defer)
+            mbar_arrive(corr_bar(s, rq));  // the correction warp arrives for us
+          else
+            mbar_arrive_cluster_relaxed(bar_l(L::PV_READY + s));
+        }
       }
       if (!ok) break;
 
@@ -303,7 +320,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t stage_buf = sOut + static_cast<uint32_t>(rq * L::kOutWarpBytes);
     uint32_t n_t0 = 0, n_t1 = 0;
     uint32_t n_e0 = 0, n_e1 = 0;
+    uint32_t n_c[2] = {0u, 0u};  // correction requests served, per stage
     bool ok = true;
+    // as in fa_prefill_kernel: the wait for 1/l serves this quarter's
+    // correction requests in the correction-warpgroup form
+    auto epi_wait = [&](uint32_t b, uint32_t par) -> bool {
+      if constexpr (!kCorrWG) {
+        return wait_bar_warp<kSleepEpilogueNs>(b, par, ctl);
+      } else {
+        uint64_t t0 = 0;
+        for (uint32_t n = 1;; ++n) {
+          if (__any_sync(0xffffffffu, mbar_test_wait(b, par))) return true;
+#pragma unroll
+          for (int s2 = 0; s2 < 2; ++s2) {
+            if (__any_sync(0xffffffffu, mbar_test_wait(corr_bar(s2, rq), n_c[s2] & 1))) {
+              tc_fence_after();
+              correct_rows<D>(tmem + t_lane + static_cast<uint32_t>(s2 * kBN),
+                              tmem + t_lane + static_cast<uint32_t>(L::kTmemO + s2 * D));
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive_cluster_relaxed(bar_l(L::PV_READY + s2));
+              ++n_c[s2];
+              t0 = 0;
+            }
+          }
+          if ((n & 7u) == 0) {
+            if (*ctl.abort) return false;
+            const uint64_t t = globaltimer_ns();
+            if (t0 == 0) {
+              t0 = t;
+            } else if (t - t0 > ctl.timeout) {
+              *ctl.abort = 1u;
+              atomicExch(ctl.status, kStatusTimeout);
+              return false;
+            }
+          }
+          __nanosleep(kSleepCorrNs);
+        }
+      }
+    };
 #pragma unroll 1
     for (uint32_t k = 0; ok; ++k) {
       const int idx = pair_take_item<kPairSleepEpilogueNs>(item_ring, bar(L::ITEM_FULL),
@@ -320,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t& n_t = s == 0 ? n_t0 : n_t1;
           uint32_t& n_e = s == 0 ? n_e0 : n_e1;
           n_t += static_cast<uint32_t>(nT);
-          if (!wait_bar_warp<kSleepEpilogueNs>(bar(L::ML_FULL + s), n_e & 1, ctl)) { ok = false; continue; }
+          if (!epi_wait(bar(L::ML_FULL + s), n_e & 1)) { ok = false; continue; }
           ++n_e;
           inv_l = inv_l_smem[s * kBM + r];
           if (!wait_bar_warp<kSleepEpilogueNs>(bar(L::O_READY + s), (n_t - 1) & 1, ctl)) { ok = false; continue; }

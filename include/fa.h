@@ -103,6 +103,14 @@ typedef enum {
                                         with at least one 512-row item per
                                         two SMs                             */
 #define FA_FLAG_SINGLE_CTA 0x10u     /* prefill: never use CTA pairs        */
+#define FA_FLAG_CORRECTION_WG 0x20u  /* prefill over the whole key range: a
+                                        dedicated correction warpgroup
+                                        rescales O in tensor memory when a
+                                        row's max moves (the softmax warps
+                                        hand it those tiles) instead of the
+                                        softmax warps doing it themselves;
+                                        same results, bitwise.  Ignored with
+                                        split keys                          */
 #define FA_FLAG_TEST_STALL 0x100u    /* test hook: the K/V producer of every
                                         CTA withholds its first item's second
                                         K tile, so the consumers' bounded

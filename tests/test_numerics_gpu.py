@@ -137,3 +137,24 @@ def test_special_values_through_the_hot_path(kernel):
     assert torch.equal(o[:, :, 100], v[:, :, 0])
     s00 = (q[:, :, 100].double() * k[:, :, 0].double()).sum(-1) * D ** -0.5
     assert (lse[:, :, 100].double() - s00).abs().max().item() < 1e-5
+
+
+@pytest.mark.parametrize("kernel", KERNELS, ids=lambda k: k[0])
+@pytest.mark.parametrize("exact", [False, True], ids=["tau8", "exact_max"])
+@pytest.mark.parametrize("always", [False, True], ids=["on_change", "every_tile"])
+def test_correction_warpgroup_form_matches_merged_form(kernel, exact, always):
+    """FA_FLAG_CORRECTION_WG: a dedicated correction warp rescales O in
+    tensor memory for the tiles whose rows moved their max (the softmax warps
+    hand those tiles over).  It multiplies each element of O by the same
+    alpha as the merged form, so the outputs are the same bits; with the
+    exact running max and on every tile the hand-over happens on most tiles.
+    Rows whose max keeps rising (the ramped keys) and x4 scores."""
+    _, D, flags = kernel
+    q, k, v = _ramped(D, "bf16", 54)
+    f = flags | (fa.FA_FLAG_EXACT_MAX if exact else 0) | \
+        (fa.FA_FLAG_ALWAYS_RESCALE if always else 0)
+    o1, l1 = run_kernel(q, k, v, True, flags=f)
+    o2, l2 = run_kernel(q, k, v, True, flags=f | fa.FA_FLAG_CORRECTION_WG)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    r = check(q, k, v, o2, l2, True, "bf16")
+    assert r.passed, str(r)

@@ -253,3 +253,38 @@ def test_watchdog_reports_timeout_and_context_survives():
         fa.fa_set_watchdog_ns(0)
     o, lse = run_kernel(q, k, v, False)
     _assert(check(q, k, v, o, lse, False, "bf16"))
+
+
+@pytest.mark.parametrize("w", [inputs.C2_X4, inputs.C2_X4_CAUSAL],
+                         ids=lambda w: w.name)
+@pytest.mark.parametrize("kflag", [fa.FA_FLAG_SINGLE_CTA, fa.FA_FLAG_PAIR],
+                         ids=["single", "pair"])
+def test_correction_warpgroup_form_all_rows(w, kflag):
+    """The correction-warpgroup form against the oracle on every row of the
+    x4 workload (scores four times larger: the reference max moves), in
+    exact-max mode so that most tiles go through the correction warps, and
+    bitwise equal to the merged form."""
+    q, k, v = w.make()
+    f = kflag | fa.FA_FLAG_EXACT_MAX
+    o1, l1 = run_kernel(q, k, v, w.causal, flags=f | fa.FA_FLAG_CORRECTION_WG)
+    _assert(check(q, k, v, o1, l1, w.causal, w.dtype))
+    o2, l2 = run_kernel(q, k, v, w.causal, flags=f)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_correction_warpgroup_watchdog():
+    """A withheld K/V tile with the correction warps polling: the watchdog
+    still ends every role and reports FA_ERR_TIMEOUT; the next call works."""
+    q, k, v = inputs.make_qkv(1, 2, 256, 512, 128, "bf16", 8)
+    dq, dk, dv = (t.cuda() for t in (q, k, v))
+    assert fa.fa_get_device_status() == fa.FA_OK
+    fa.fa_set_watchdog_ns(20_000_000)
+    try:
+        for kflag in (fa.FA_FLAG_SINGLE_CTA, fa.FA_FLAG_PAIR):
+            fa.fa_fwd_ex(dq, dk, dv, flags=kflag | fa.FA_FLAG_CORRECTION_WG |
+                         fa.FA_FLAG_TEST_STALL)
+            assert fa.fa_get_device_status() == fa.FA_ERR_TIMEOUT
+    finally:
+        fa.fa_set_watchdog_ns(0)
+    o, lse = run_kernel(q, k, v, False, flags=fa.FA_FLAG_CORRECTION_WG)
+    _assert(check(q, k, v, o, lse, False, "bf16"))
