@@ -80,6 +80,8 @@ struct DeviceState {
   // (two-CTA clusters) that fit on the device at once, per dtype
   bool pair_checked[2] = {};
   int pair_slots[2] = {};  // 0: not usable
+  bool pair64_checked[2] = {};
+  int pair64_slots[2] = {};  // the 64-key pair kernel; 0: not usable
   // fa_fwd's workspaces for split partials, one per stream handle (calls on
   // one stream run in order; calls on different streams may overlap)
   struct StreamWorkspace {
@@ -274,23 +276,34 @@ fa_status_t run_prefill_pair(DeviceState& d, const void* q, const void* k, const
                              int causal, bool bf16, unsigned flags, bool captured,
                              cudaStream_t stream) {
   const int ti = bf16 ? 1 : 0;
+  const bool k64 = (flags & FA_FLAG_PAIR64) != 0;
   {
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!d.pair_checked[ti]) {
+    if (!k64 && !d.pair_checked[ti]) {
       int regs = 0, n = 0;
       if (fa::prefill_pair_num_regs(bf16, &regs) != cudaSuccess) return FA_ERR_CUDA;
       if (regs == 128 && fa::prefill_pair_max_pairs(bf16, &n) != cudaSuccess) return FA_ERR_CUDA;
       d.pair_checked[ti] = true;
       d.pair_slots[ti] = regs == 128 ? n : 0;
     }
-    if (d.pair_slots[ti] <= 0) return FA_ERR_UNSUPPORTED;
+    if (k64 && !d.pair64_checked[ti]) {
+      int regs = 0, n = 0;
+      if (fa::prefill_pair64_num_regs(bf16, &regs) != cudaSuccess) return FA_ERR_CUDA;
+      if (regs == 128 && fa::prefill_pair64_max_pairs(bf16, &n) != cudaSuccess) return FA_ERR_CUDA;
+      d.pair64_checked[ti] = true;
+      d.pair64_slots[ti] = regs == 128 ? n : 0;
+    }
+    if ((k64 ? d.pair64_slots[ti] : d.pair_slots[ti]) <= 0) return FA_ERR_UNSUPPORTED;
   }
   constexpr int D = 128;
+  // a CTA loads half of every key tile (64 of 128 keys, or 32 of 64) and
+  // half of every value tile's columns (all of its 128 or 64 keys)
+  const int key_tile = k64 ? 64 : fa::kBN;
   CUtensorMap tq, tk, tv, to;
   fa_status_t st;
   if ((st = encode_3d(&tq, q, D, Sq, BH, fa::kBM, bf16)) != FA_OK) return st;
-  if ((st = encode_3d(&tk, k, D, Skv, BH, fa::kBN / 2, bf16)) != FA_OK) return st;  // a CTA's 64 keys
-  if ((st = encode_3d(&tv, v, D, Skv, BH, fa::kBN, bf16)) != FA_OK) return st;
+  if ((st = encode_3d(&tk, k, D, Skv, BH, key_tile / 2, bf16)) != FA_OK) return st;
+  if ((st = encode_3d(&tv, v, D, Skv, BH, key_tile, bf16)) != FA_OK) return st;
   if ((st = encode_3d(&to, o, D, Sq, BH, 32, bf16)) != FA_OK) return st;
   fa::PrefillParams p{};
   p.lse = lse;
@@ -312,10 +325,13 @@ fa_status_t run_prefill_pair(DeviceState& d, const void* q, const void* k, const
   if (n_items > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
   p.n_items = static_cast<int>(n_items);
   p.sched = sched_slot(d, captured);
-  const int n_pairs = static_cast<int>(std::min<long long>(n_items, d.pair_slots[ti]));
-  if (fa::launch_prefill_pair(bf16, (flags & FA_FLAG_CORRECTION_WG) != 0, tq, tk, tv, to, p,
-                              n_pairs, stream) != cudaSuccess)
-    return FA_ERR_CUDA;
+  const int n_pairs = static_cast<int>(
+      std::min<long long>(n_items, k64 ? d.pair64_slots[ti] : d.pair_slots[ti]));
+  const cudaError_t e =
+      k64 ? fa::launch_prefill_pair64(bf16, tq, tk, tv, to, p, n_pairs, stream)
+          : fa::launch_prefill_pair(bf16, (flags & FA_FLAG_CORRECTION_WG) != 0, tq, tk, tv, to,
+                                    p, n_pairs, stream);
+  if (e != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;
 }
 
@@ -340,7 +356,8 @@ fa_status_t run_prefill(DeviceState& d, const void* q, const void* k, const void
   }
   const int BH = B * H;
   if (D == 128 && num_splits <= 1 && !(flags & FA_FLAG_SINGLE_CTA) &&
-      ((flags & FA_FLAG_PAIR) || pair_by_default(BH, Sq, Skv, causal, d.sm_count)))
+      ((flags & (FA_FLAG_PAIR | FA_FLAG_PAIR64)) ||
+       pair_by_default(BH, Sq, Skv, causal, d.sm_count)))
     return run_prefill_pair(d, q, k, v, o, lse, BH, Sq, Skv, scale, causal, bf16, flags,
                             captured, stream);
   CUtensorMap tq, tk, tv, to;
@@ -682,7 +699,7 @@ int fa_prefill_uses_pairs(int B, int H, int Sq, int Skv, int D, int causal, unsi
   if (B <= 0 || H <= 0 || Sq <= 1 || Skv <= 0 || D != 128 || num_splits > 1 ||
       (flags & FA_FLAG_SINGLE_CTA))
     return 0;
-  if (flags & FA_FLAG_PAIR) return 1;
+  if (flags & (FA_FLAG_PAIR | FA_FLAG_PAIR64)) return 1;
   int sms = 0;
   DeviceState* d = nullptr;
   if (current_device(&d, nullptr) == FA_OK) sms = d->sm_count;

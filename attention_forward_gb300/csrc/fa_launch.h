@@ -26,6 +26,13 @@ cudaError_t launch_prefill_pair(bool bf16, bool corr, const CUtensorMap& q,
                                 const CUtensorMap& o, const PrefillParams& p, int n_pairs,
                                 cudaStream_t stream);
 
+// The CTA-pair kernel with 64-key score tiles, two score buffers per stage.
+cudaError_t prefill_pair64_num_regs(bool bf16, int* regs);
+cudaError_t prefill_pair64_max_pairs(bool bf16, int* n);
+cudaError_t launch_prefill_pair64(bool bf16, const CUtensorMap& q, const CUtensorMap& k,
+                                  const CUtensorMap& v, const CUtensorMap& o,
+                                  const PrefillParams& p, int n_pairs, cudaStream_t stream);
+
 int decode_smem_bytes(int D);
 cudaError_t launch_decode(int D, bool bf16, const DecodeParams& p, int grid,
                           cudaStream_t stream);

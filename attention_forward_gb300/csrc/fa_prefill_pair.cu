@@ -5,6 +5,7 @@
 
 #include "fa_launch.h"
 #include "fa_prefill_pair.cuh"
+#include "fa_prefill_pair64.cuh"
 
 namespace fa {
 namespace {
@@ -76,7 +77,69 @@ cudaError_t num_regs(int* regs) {
   return e;
 }
 
+// The 64-key kernel (fa_prefill_pair64.cuh).
+template <bool BF16>
+cudaError_t set_attrs64() {
+  static std::mutex mu;
+  static bool done[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(fa_prefill_pair64_kernel<BF16>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, Pair64Layout::kSmemBytes);
+  if (e == cudaSuccess) done[dev] = true;
+  return e;
+}
+
+template <bool BF16>
+cudaError_t launch64(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                     const CUtensorMap& o, const PrefillParams& p, int n_pairs,
+                     cudaStream_t stream) {
+  cudaError_t e = set_attrs64<BF16>();
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pair_config(2 * n_pairs, stream, attr);
+  cfg.dynamicSmemBytes = Pair64Layout::kSmemBytes;
+  return cudaLaunchKernelEx(&cfg, fa_prefill_pair64_kernel<BF16>, q, k, v, o, p);
+}
+
+template <bool BF16>
+cudaError_t max_pairs64(int* n) {
+  cudaError_t e = set_attrs64<BF16>();
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pair_config(2, nullptr, attr);
+  cfg.dynamicSmemBytes = Pair64Layout::kSmemBytes;
+  return cudaOccupancyMaxActiveClusters(n, fa_prefill_pair64_kernel<BF16>, &cfg);
+}
+
+template <bool BF16>
+cudaError_t num_regs64(int* regs) {
+  cudaFuncAttributes a{};
+  const cudaError_t e = cudaFuncGetAttributes(&a, fa_prefill_pair64_kernel<BF16>);
+  if (e == cudaSuccess) *regs = a.numRegs;
+  return e;
+}
+
 }  // namespace
+
+cudaError_t prefill_pair64_max_pairs(bool bf16, int* n) {
+  return bf16 ? max_pairs64<true>(n) : max_pairs64<false>(n);
+}
+
+cudaError_t prefill_pair64_num_regs(bool bf16, int* regs) {
+  return bf16 ? num_regs64<true>(regs) : num_regs64<false>(regs);
+}
+
+cudaError_t launch_prefill_pair64(bool bf16, const CUtensorMap& q, const CUtensorMap& k,
+                                  const CUtensorMap& v, const CUtensorMap& o,
+                                  const PrefillParams& p, int n_pairs, cudaStream_t stream) {
+  return bf16 ? launch64<true>(q, k, v, o, p, n_pairs, stream)
+              : launch64<false>(q, k, v, o, p, n_pairs, stream);
+}
 
 cudaError_t prefill_pair_max_pairs(bool bf16, int* n) {
   return bf16 ? max_pairs<true>(n) : max_pairs<false>(n);

@@ -499,6 +499,31 @@ __device__ __forceinline__ void umma_pair_ts_k128(uint32_t d_tmem, uint32_t a_tm
       : "memory");
 }
 
+// Four K=16 steps of a pair MMA with A in tensor memory (a K = 64
+// contraction: 8 columns of packed 16-bit pairs per step) and B MN-major
+// 128-byte swizzled in shared memory (16 K rows = 128 descriptor units per
+// step).
+__device__ __forceinline__ void umma_pair_ts_k64(uint32_t d_tmem, uint32_t a_tmem,
+                                                 uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e, t;\n\t"
+      ".reg .b32 a1, a2, a3;\n\t"
+      ".reg .b64 b1, b2, b3;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 t, 0, 0;\n\t"
+      "add.s32 a1, %1, 8;\n\t  add.s64 b1, %2, 128;\n\t"
+      "add.s32 a2, %1, 16;\n\t add.s64 b2, %2, 256;\n\t"
+      "add.s32 a3, %1, 24;\n\t add.s64 b3, %2, 384;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [a1], b1, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [a2], b2, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [a3], b3, %3, t;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on the mbarrier at shared offset `bar` in each CTA of
 // `cta_mask` when every pair MMA issued so far by the elected lane has
 // completed.

@@ -111,6 +111,13 @@ typedef enum {
                                         softmax warps doing it themselves;
                                         same results, bitwise.  Ignored with
                                         split keys                          */
+#define FA_FLAG_PAIR64 0x40u         /* prefill, D = 128, without a key
+                                        split: CTA pairs with score tiles of
+                                        64 keys and two score buffers per
+                                        stage, so that the next tile's
+                                        scores are computed while the
+                                        softmax of this one runs; ignored
+                                        where FA_FLAG_PAIR would be         */
 #define FA_FLAG_TEST_STALL 0x100u    /* test hook: the K/V producer of every
                                         CTA withholds its first item's second
                                         K tile, so the consumers' bounded
