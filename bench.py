@@ -72,6 +72,9 @@ def parse_args(argv=None):
     ap.add_argument("--prefill-kernel", default="auto", choices=["auto", "single", "pair"],
                     help="prefill kernel: the library's choice (default), single CTAs "
                          "(FA_FLAG_SINGLE_CTA) or CTA pairs (FA_FLAG_PAIR)")
+    ap.add_argument("--extra-flags", type=lambda x: int(x, 0), default=0,
+                    help="FA_FLAG_* bits added to every call of this run (e.g. 0x20 for "
+                         "the correction-warpgroup form)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--ref-seconds", type=float, default=120.0,
@@ -575,8 +578,8 @@ def result_line(prob, K, warmup, world, total_max, launch_ms, clocks):
     }
 
 
-def kernel_flags(fa, name):
-    return {"auto": 0, "single": fa.FA_FLAG_SINGLE_CTA, "pair": fa.FA_FLAG_PAIR}[name]
+def kernel_flags(fa, name, extra=0):
+    return {"auto": 0, "single": fa.FA_FLAG_SINGLE_CTA, "pair": fa.FA_FLAG_PAIR}[name] | extra
 
 
 def bench_ours(args, w):
@@ -591,7 +594,7 @@ def bench_ours(args, w):
     fa.load()
     stream = torch.cuda.current_stream(device)
     prob = Problem(w, device, stream, seed=shard_seed(w.seed, rank),
-                   kflags=kernel_flags(fa, args.prefill_kernel))
+                   kflags=kernel_flags(fa, args.prefill_kernel, args.extra_flags))
     K = args.steps
     total_s, launch_ms, clocks = timed_steps(prob, K, args.warmup, world)
     total_max = max_over_ranks(total_s, world, device)
@@ -639,7 +642,7 @@ def bench_sweep(args):
     for w in inputs.CONFIGURED:
         if names and w.name not in names:
             continue
-        prob = Problem(w, device, stream, kflags=kernel_flags(fa, args.prefill_kernel))
+        prob = Problem(w, device, stream, kflags=kernel_flags(fa, args.prefill_kernel, args.extra_flags))
         # size the run: a few probe steps first
         for _ in range(3):
             prob.step()
