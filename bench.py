@@ -690,6 +690,29 @@ def paired_margins(prob, arms, alternations, pwarm, pmeasure):
     return out
 
 
+def paired_summary(res):
+    """Statistics of paired alternations [(median_A_ms, median_B_ms, "AB"|"BA")]:
+    the per-alternation margin t_A / t_B (> 1: B faster), its median,
+    geometric mean and p10/p90, the median of each order half, B's wins."""
+    m = np.array([a / b for a, b, _ in res])
+    half = lambda o: float(np.median([a / b for a, b, oo in res if oo == o]))
+    return {
+        "margin": float(np.median(m)),
+        "margin_gmean": float(np.exp(np.mean(np.log(m)))),
+        "paired_lo": float(np.percentile(m, 10)), "paired_hi": float(np.percentile(m, 90)),
+        "ab_half": half("AB"), "ba_half": half("BA"),
+        "b_wins": int((m > 1).sum()), "alternations": len(res),
+        "t_a_ms": float(np.median([a for a, _, _ in res])),
+        "t_b_ms": float(np.median([b for _, b, _ in res])),
+    }
+
+
+def aa_noise(margins):
+    """The A/A null's noise floor: p95 of |margin - 1| (and its maximum)."""
+    dev = np.abs(np.asarray(margins, dtype=np.float64) - 1.0)
+    return float(np.percentile(dev, 95)), float(dev.max())
+
+
 def bench_paired(args, w):
     """Paired, interleaved A/B of two arms on one workload (see the module
     docstring); prints one JSON line."""
@@ -718,19 +741,11 @@ def bench_paired(args, w):
     sampler.stop()
     if fa.fa_get_device_status() != fa.FA_OK:
         raise RuntimeError("kernel watchdog fired in a paired run")
-    m = np.array([a / b for a, b, _ in res])
-    half = lambda o: float(np.median([a / b for a, b, oo in res if oo == o]))
     line = {
         "mode": "paired", "workload": w.name,
         "a": {"flags": args.a_flags, "lib": args.a_lib or "in-tree", "tag": args.a_tag},
         "b": {"flags": args.b_flags, "lib": args.b_lib or "in-tree", "tag": args.b_tag},
-        "margin": float(np.median(m)),
-        "margin_gmean": float(np.exp(np.mean(np.log(m)))),
-        "paired_lo": float(np.percentile(m, 10)), "paired_hi": float(np.percentile(m, 90)),
-        "ab_half": half("AB"), "ba_half": half("BA"),
-        "b_wins": int((m > 1).sum()), "alternations": len(res),
-        "t_a_ms": float(np.median([a for a, _, _ in res])),
-        "t_b_ms": float(np.median([b for _, b, _ in res])),
+        **paired_summary(res),
         "protocol": f"{args.alternations} alternations x ({args.pwarm} warm-up + "
                     f"{args.pmeasure} timed launches per arm), order AB/BA alternating; "
                     "margin = median_A / median_B per alternation (> 1: B faster)",
@@ -755,11 +770,10 @@ def bench_aa(args, w):
         margins.append(d["margin"])
         lines.append({k: d[k] for k in ("margin", "ab_half", "ba_half", "b_wins",
                                         "t_a_ms", "t_b_ms")} | {"sm_mhz": d["clocks"]["sm_mhz"]})
-    dev = np.abs(np.array(margins) - 1.0)
-    t_noise = float(np.percentile(dev, 95))
+    t_noise, t_max = aa_noise(margins)
     print(json.dumps({"mode": "aa_null", "workload": w.name, "runs": len(margins),
                       "margins": margins, "t_noise": t_noise,
-                      "t_noise_max": float(dev.max()), "t_keep": 1.0 + t_noise,
+                      "t_noise_max": t_max, "t_keep": 1.0 + t_noise,
                       "protocol": f"{args.alternations} alternations x ({args.pwarm} + "
                                   f"{args.pmeasure} launches per arm), each run a fresh "
                                   "process, both arms the in-tree build",

@@ -95,3 +95,39 @@ def test_kernel_fingerprint_covers_device_code_only(tmp_path, monkeypatch):
     dev = dst / "fa_prefill_pair.cuh"
     dev.write_text(dev.read_text() + "\n// a device-side edit\n")
     assert bench.kernel_fingerprint() != f0
+
+
+def test_paired_summary_margins_and_halves():
+    """margin = t_A / t_B per alternation; its median, the AB and BA halves
+    and B's wins; B 2 % faster in every alternation gives margin 1/0.98."""
+    res = [(1.0, 0.98, "AB" if i % 2 == 0 else "BA") for i in range(10)]
+    d = bench.paired_summary(res)
+    assert d["margin"] == pytest.approx(1 / 0.98)
+    assert d["ab_half"] == pytest.approx(1 / 0.98) and d["ba_half"] == pytest.approx(1 / 0.98)
+    assert d["b_wins"] == 10 and d["alternations"] == 10
+    # an order effect shows in the halves, not in the median of both
+    res = [(1.0, 0.99, "AB"), (1.0, 1.01, "BA")] * 5
+    d = bench.paired_summary(res)
+    assert d["ab_half"] > 1 > d["ba_half"] and d["b_wins"] == 5
+
+
+def test_aa_noise_is_the_p95_of_the_deviation():
+    t, mx = bench.aa_noise([1.0, 1.001, 0.999, 1.0, 1.0, 1.0005, 0.9998, 1.0, 1.0, 0.997])
+    assert mx == pytest.approx(0.003)
+    assert 0.001 <= t <= 0.003
+
+
+def test_clock_summary_counts_only_samples_inside_the_region():
+    """Clock samples outside the timed region are never used, and a region
+    with fewer than three samples is marked."""
+    c = bench.NvmlClocks.__new__(bench.NvmlClocks)
+    c.ok, c.max_mhz = True, 2070.0
+    c.samples = [(0.5, 1000.0, 150.0, 0), (1.1, 1980.0, 900.0, 0x4),
+                 (1.2, 1995.0, 950.0, 0), (1.3, 2010.0, 980.0, 0), (9.0, 900.0, 100.0, 0x8)]
+    d = c.summary(1.0, 2.0)
+    assert d["samples"] == 3 and d["sm_mhz"] == 1995.0 and d["sm_mhz_min"] == 1980.0
+    assert d["reasons"] == ["sw_power_cap"] and "note" not in d
+    d = c.summary(1.15, 1.25)
+    assert d["samples"] == 1 and "fewer than 3" in d["note"]
+    d = c.summary(3.0, 4.0)
+    assert d["samples"] == 0 and d["sm_mhz"] is None
