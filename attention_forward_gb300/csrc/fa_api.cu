@@ -317,6 +317,8 @@ fa_status_t run_prefill_pair(DeviceState& d, const void* q, const void* k, const
   p.lpt = (flags & FA_FLAG_NO_LPT) ? 0 : 1;
   p.always_rescale = (flags & FA_FLAG_ALWAYS_RESCALE) ? 1 : 0;
   p.test_stall = (flags & FA_FLAG_TEST_STALL) ? 1 : 0;
+  // the 64-key pair kernel has no programmatic-launch waits: never overlapped
+  p.overlap_prev = (flags & FA_FLAG_OVERLAP_PREVIOUS) && !k64 ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.rescale_tau = (flags & FA_FLAG_EXACT_MAX) ? 0.f : 8.f;
   p.n_splits = 1;
@@ -377,6 +379,7 @@ fa_status_t run_prefill(DeviceState& d, const void* q, const void* k, const void
   p.lpt = (flags & FA_FLAG_NO_LPT) ? 0 : 1;
   p.always_rescale = (flags & FA_FLAG_ALWAYS_RESCALE) ? 1 : 0;
   p.test_stall = (flags & FA_FLAG_TEST_STALL) ? 1 : 0;
+  p.overlap_prev = (flags & FA_FLAG_OVERLAP_PREVIOUS) ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.rescale_tau = (flags & FA_FLAG_EXACT_MAX) ? 0.f : 8.f;
   const int n_tiles = (Skv + fa::kBN - 1) / fa::kBN;

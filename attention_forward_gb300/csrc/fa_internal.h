@@ -49,6 +49,9 @@ struct PrefillParams {
   int tiles_per_split;        // key tiles of kBN per range
   float* part_o;              // n_splits > 1: [n_splits, BH*Sq, D] fp32, O / l
   float* part_lse;            // n_splits > 1: [n_splits, BH*Sq] fp32
+  // launched to overlap the previous grid on the stream: every thread waits
+  // for it before its first global write (reads of Q, K, V may start early)
+  int overlap_prev;
 };
 
 // Decode (Sq == 1) split-KV.

@@ -578,6 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = tmem + t_lane + static_cast<uint32_t>(L::kTmemO + s * D);
     uint32_t n_s = 0;  // tiles of this stage so far (S_FULL / O_READY phase)
     bool ok = true;
+    bool dep_wait = p.overlap_prev != 0;  // before the first global write
 
 #pragma unroll 1
     for (uint32_t k = 0; ok; ++k) {
@@ -606,6 +607,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // end of the item: LSE straight to global, 1/l to the epilogue warps
       // once the item's last PV_s has completed (then O_s is final)
+      if (dep_wait) {
+        grid_dependency_wait();
+        dep_wait = false;
+      }
       if (row_g < p.Sq) {
         const float lse = l > 0.f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
         if constexpr (kSplit)
@@ -635,6 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t n_e0 = 0, n_e1 = 0;  // ML_FULL phases
     uint32_t n_c[2] = {0u, 0u};   // correction requests served, per stage
     bool ok = true;
+    bool dep_wait = p.overlap_prev != 0;  // before the first global write
     // The wait for an item's 1/l (the end of its stage): in the
     // correction-warpgroup form it also serves this quarter's correction
     // requests of both stages, polling without suspending; bounded by the
@@ -680,6 +686,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                   bar(L::ITEM_EMPTY), k, ctl, ok);
       if (!ok || idx < 0) break;
       const ItemT<kSplit> it = get_item<kSplit>(p, idx);
+      if (dep_wait) {
+        grid_dependency_wait();
+        dep_wait = false;
+      }
 #pragma unroll
       for (int s = 0; s < 2; ++s) {
         if (!ok) continue;
@@ -980,6 +990,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok && it.nT1 == 0) ok = load_q(it, 1);
         idx = claim_item(p);
+        if (idx < 0) grid_launch_dependents();  // the next grid may take the SMs
       }
       // drain: every load issued lands before shared memory goes away
 #pragma unroll

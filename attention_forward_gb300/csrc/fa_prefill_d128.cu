@@ -33,9 +33,19 @@ cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k,
                    const PrefillParams& p, int grid, cudaStream_t stream) {
   cudaError_t e = set_smem_attr<BF16, kSplit, kCorr>();
   if (e != cudaSuccess) return e;
-  fa_prefill_kernel<128, BF16, kSplit, kCorr><<<grid, kThreads, PrefillLayout<128>::kSmemBytes,
-                                        stream>>>(q, k, v, o, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = PrefillLayout<128>::kSmemBytes;
+  cfg.stream = stream;
+  // overlap with the previous grid on the stream (programmatic dependent
+  // launch): the kernel waits for it before its first global write
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.overlap_prev ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, fa_prefill_kernel<128, BF16, kSplit, kCorr>, q, k, v, o, p);
 }
 
 template <bool BF16, bool kSplit, bool kCorr = false>

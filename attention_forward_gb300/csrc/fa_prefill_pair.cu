@@ -26,7 +26,11 @@ cudaError_t set_attrs() {
   return e;
 }
 
-cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribute* attr) {
+// attr must hold 2 entries: the cluster shape, and (overlap) programmatic
+// stream serialization: the kernel then overlaps the previous grid on the
+// stream and waits for it before its first global write.
+cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribute* attr,
+                               bool overlap = false) {
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -36,8 +40,10 @@ cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribut
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = overlap ? 2 : 1;
   return cfg;
 }
 
@@ -47,8 +53,8 @@ cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap
                    cudaStream_t stream) {
   cudaError_t e = set_attrs<BF16, kCorr>();
   if (e != cudaSuccess) return e;
-  cudaLaunchAttribute attr[1];
-  const cudaLaunchConfig_t cfg = pair_config(2 * n_pairs, stream, attr);
+  cudaLaunchAttribute attr[2];
+  const cudaLaunchConfig_t cfg = pair_config(2 * n_pairs, stream, attr, p.overlap_prev != 0);
   return cudaLaunchKernelEx(&cfg, fa_prefill_pair_kernel<BF16, kCorr>, q, k, v, o, p);
 }
 
@@ -60,7 +66,7 @@ cudaError_t max_pairs(int* n) {
   if (e != cudaSuccess) return e;
   e = set_attrs<BF16, true>();
   if (e != cudaSuccess) return e;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   const cudaLaunchConfig_t cfg = pair_config(2, nullptr, attr);
   return cudaOccupancyMaxActiveClusters(n, fa_prefill_pair_kernel<BF16, false>, &cfg);
 }
@@ -100,7 +106,7 @@ cudaError_t launch64(const CUtensorMap& q, const CUtensorMap& k, const CUtensorM
                      cudaStream_t stream) {
   cudaError_t e = set_attrs64<BF16>();
   if (e != cudaSuccess) return e;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = pair_config(2 * n_pairs, stream, attr);
   cfg.dynamicSmemBytes = Pair64Layout::kSmemBytes;
   return cudaLaunchKernelEx(&cfg, fa_prefill_pair64_kernel<BF16>, q, k, v, o, p);
@@ -110,7 +116,7 @@ template <bool BF16>
 cudaError_t max_pairs64(int* n) {
   cudaError_t e = set_attrs64<BF16>();
   if (e != cudaSuccess) return e;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = pair_config(2, nullptr, attr);
   cfg.dynamicSmemBytes = Pair64Layout::kSmemBytes;
   return cudaOccupancyMaxActiveClusters(n, fa_prefill_pair64_kernel<BF16>, &cfg);

@@ -268,6 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = tmem + t_lane + static_cast<uint32_t>(L::kTmemO + s * D);
     uint32_t n_s = 0;
     bool ok = true;
+    bool dep_wait = p.overlap_prev != 0;  // before the first global write
 
 #pragma unroll 1
     for (uint32_t k = 0; ok; ++k) {
@@ -300,6 +301,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
 
+      if (dep_wait) {
+        grid_dependency_wait();
+        dep_wait = false;
+      }
       if (row_g < p.Sq) {
         const float lse = l > 0.f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
         p.lse[static_cast<size_t>(it.bh) * p.Sq + row_g] = lse;
@@ -322,6 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t n_e0 = 0, n_e1 = 0;
     uint32_t n_c[2] = {0u, 0u};  // correction requests served, per stage
     bool ok = true;
+    bool dep_wait = p.overlap_prev != 0;  // before the first global write
     // as in fa_prefill_kernel: the wait for 1/l serves this quarter's
     // correction requests in the correction-warpgroup form
     auto epi_wait = [&](uint32_t b, uint32_t par) -> bool {
@@ -365,6 +371,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                            bar_l(L::ITEM_EMPTY), k, ctl, ok);
       if (!ok || idx < 0) break;
       const PairItem it = get_pair_item(p, idx);
+      if (dep_wait) {
+        grid_dependency_wait();
+        dep_wait = false;
+      }
 #pragma unroll
       for (int s = 0; s < 2; ++s) {
         if (!ok) continue;
@@ -632,7 +642,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           idx = item_ring[slot];
           mbar_arrive_cluster(bar_l(L::ITEM_EMPTY + slot));
         }
-        if (idx < 0) break;
+        if (idx < 0) {
+          grid_launch_dependents();  // the next grid may take the SMs
+          break;
+        }
         const PairItem it = get_pair_item(p, idx);
         ok = load_q(it, 0);
 #pragma unroll 1

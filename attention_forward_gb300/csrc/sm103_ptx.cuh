@@ -85,6 +85,22 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// ------------------------------------------------------------ launches
+
+// Programmatic dependent launch: this CTA has no more work to claim, so the
+// next grid on the stream (launched with programmatic stream serialization)
+// may start once every CTA of this grid has signalled or exited.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Blocks until the grids this one depends on (programmatically) have
+// completed and their memory operations are visible; returns at once when
+// there is none.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ------------------------------------------------------------ proxies
 
 // Order this thread's generic-proxy shared-memory writes before later

@@ -26,6 +26,7 @@ FA_FLAG_PAIR = 0x8
 FA_FLAG_SINGLE_CTA = 0x10
 FA_FLAG_CORRECTION_WG = 0x20
 FA_FLAG_PAIR64 = 0x40
+FA_FLAG_OVERLAP_PREVIOUS = 0x80
 FA_FLAG_TEST_STALL = 0x100
 
 _DTYPE = {torch.float16: FA_F16, torch.bfloat16: FA_BF16}

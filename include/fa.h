@@ -118,6 +118,21 @@ typedef enum {
                                         scores are computed while the
                                         softmax of this one runs; ignored
                                         where FA_FLAG_PAIR would be         */
+#define FA_FLAG_OVERLAP_PREVIOUS 0x80u /* prefill: launch so that the kernel
+                                        may start while the previous grid on
+                                        `stream` is still running (CUDA
+                                        programmatic dependent launch): it
+                                        reads q, k, v at once but waits for
+                                        that grid before its first write of
+                                        o, lse or the workspace.  The caller
+                                        guarantees that the work before it
+                                        on the stream does not write q, k or
+                                        v (e.g. back-to-back calls on
+                                        resident inputs).  The library's own
+                                        prefill kernels let the next grid
+                                        start as soon as their SMs run out
+                                        of work items.  Ignored by decode
+                                        and FA_FLAG_PAIR64                  */
 #define FA_FLAG_TEST_STALL 0x100u    /* test hook: the K/V producer of every
                                         CTA withholds its first item's second
                                         K tile, so the consumers' bounded
