@@ -9,6 +9,11 @@
 A step is one forward pass (every step of the hot path) over one batch of
 synthetic input already resident in HBM.  The default workload is
 B=4, H=16, Sq=Skv=4096, D=128, bf16, non-causal.  Rank 0 prints one JSON line.
+For prefill the line's value times back-to-back fa_fwd_ex calls with
+FA_FLAG_OVERLAP_PREVIOUS (programmatic dependent launch: a step starts on
+the SMs the previous one has run out of work for and waits for it before
+its first write); the same K steps as plain fa_fwd calls, timed step by
+step, are its `plain` entry.  --no-overlap times the plain calls only.
 
 Multi-GPU (torchrun, one process per GPU): every rank runs its own batch of
 the same shape (independent heads, no data-path collective), so scaling is
@@ -69,6 +74,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-gemm-ceiling", action="store_true")
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="time plain fa_fwd steps only (no programmatic dependent launch)")
     ap.add_argument("--prefill-kernel", default="auto", choices=["auto", "single", "pair"],
                     help="prefill kernel: the library's choice (default), single CTAs "
                          "(FA_FLAG_SINGLE_CTA) or CTA pairs (FA_FLAG_PAIR)")
@@ -514,11 +521,13 @@ class Problem:
                            lse=self.lse, stream=self.stream)
 
 
-def timed_steps(prob, K, warmup, world=1, sampler=None):
+def timed_steps(prob, K, warmup, world=1, sampler=None, per_step=True):
     """W untimed steps, then exactly K steps bracketed by a barrier and a
     synchronize on both sides, with CUDA events on the launching stream
-    around the whole region and around every step.  Returns (seconds of the
-    region, sorted per-step ms, clock summary)."""
+    around the whole region and (per_step) around every step.  Without
+    per-step events consecutive steps may overlap (an event between two
+    launches would serialise them); every step's time is then the region's
+    over K.  Returns (seconds of the region, sorted per-step ms, clocks)."""
     fa, device, stream = prob.fa, prob.device, prob.stream
     for _ in range(max(3, warmup)):
         prob.step()
@@ -537,9 +546,11 @@ def timed_steps(prob, K, warmup, world=1, sampler=None):
     wall0 = time.time()
     t_start.record(stream)
     for i in range(K):
-        ev[i][0].record(stream)
+        if per_step:
+            ev[i][0].record(stream)
         prob.step()
-        ev[i][1].record(stream)
+        if per_step:
+            ev[i][1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize(device)
     wall1 = time.time()
@@ -550,7 +561,10 @@ def timed_steps(prob, K, warmup, world=1, sampler=None):
     if fa.fa_get_device_status() != fa.FA_OK:
         raise RuntimeError("kernel watchdog fired in the timed region")
     total_s = t_start.elapsed_time(t_end) / 1e3
-    launch_ms = sorted(a.elapsed_time(b) for a, b in ev)
+    if per_step:
+        launch_ms = sorted(a.elapsed_time(b) for a, b in ev)
+    else:
+        launch_ms = [total_s * 1e3 / K] * K
     return total_s, launch_ms, clocks
 
 
@@ -573,13 +587,50 @@ def result_line(prob, K, warmup, world, total_max, launch_ms, clocks):
         "roofline": roof,
         "gpu_launches": K * launches_per_step(fa, w),
         "step_ms": {"mean": launch_s * 1e3, "median": statistics.median(launch_ms),
-                    "p10": pct(0.10), "p90": pct(0.90), "source": "CUDA events around each step"},
+                    "p10": pct(0.10), "p90": pct(0.90),
+                    "source": ("CUDA events around each step" if len(set(launch_ms)) > 1 or K == 1
+                               else "CUDA events around the region, over K (steps overlap)")},
         "clocks": clocks,
     }
 
 
 def kernel_flags(fa, name, extra=0):
     return {"auto": 0, "single": fa.FA_FLAG_SINGLE_CTA, "pair": fa.FA_FLAG_PAIR}[name] | extra
+
+
+OVERLAP_NOTE = ("back-to-back fa_fwd_ex calls with FA_FLAG_OVERLAP_PREVIOUS (CUDA programmatic "
+                "dependent launch): a step's CTAs start on the SMs the previous step has run out "
+                "of work for, read the resident inputs at once and wait for the previous step "
+                "before their first write; every step computes the whole forward pass; timed "
+                "with events around the region only")
+
+
+def measure(prob, K, warmup, world, device, overlap):
+    """The line of one workload: with overlap (prefill), K overlapped steps
+    are the line's value and K plain fa_fwd steps, timed with per-step
+    events, its `plain` entry; without (or for decode, which the flag does
+    not change), the plain steps alone."""
+    fa = prob.fa
+    base = prob.kflags
+    total_p, ms_p, clocks_p = timed_steps(prob, K, warmup, world)
+    total_p = max_over_ranks(total_p, world, device)
+    plain = result_line(prob, K, warmup, world, total_p, ms_p, clocks_p)
+    if not overlap or prob.w.Sq == 1:
+        plain["launch"] = "back-to-back fa_fwd calls, CUDA events around each step"
+        return plain
+    prob.kflags = base | fa.FA_FLAG_OVERLAP_PREVIOUS
+    try:
+        total_o, ms_o, clocks_o = timed_steps(prob, K, warmup, world, per_step=False)
+    finally:
+        prob.kflags = base
+    total_o = max_over_ranks(total_o, world, device)
+    line = result_line(prob, K, warmup, world, total_o, ms_o, clocks_o)
+    line["launch"] = OVERLAP_NOTE
+    line["plain"] = {"value": plain["value"], "ms_per_step": plain["ms_per_step"],
+                     "roofline_frac": plain["roofline"]["frac"], "step_ms": plain["step_ms"],
+                     "clocks": plain["clocks"],
+                     "launch": "back-to-back fa_fwd calls, CUDA events around each step"}
+    return line
 
 
 def bench_ours(args, w):
@@ -596,9 +647,7 @@ def bench_ours(args, w):
     prob = Problem(w, device, stream, seed=shard_seed(w.seed, rank),
                    kflags=kernel_flags(fa, args.prefill_kernel, args.extra_flags))
     K = args.steps
-    total_s, launch_ms, clocks = timed_steps(prob, K, args.warmup, world)
-    total_max = max_over_ranks(total_s, world, device)
-    line = result_line(prob, K, args.warmup, world, total_max, launch_ms, clocks)
+    line = measure(prob, K, args.warmup, world, device, not args.no_overlap)
     decode = w.Sq == 1
 
     if not args.no_e2e:
@@ -653,8 +702,7 @@ def bench_sweep(args):
         torch.cuda.synchronize(device)
         per = (time.perf_counter() - t0) / 5
         K = int(min(5000, max(20, args.sweep_seconds / max(per, 1e-6))))
-        total_s, launch_ms, clocks = timed_steps(prob, K, args.warmup, 1)
-        line = result_line(prob, K, args.warmup, 1, total_s, launch_ms, clocks)
+        line = measure(prob, K, args.warmup, 1, device, not args.no_overlap)
         if gemm is not None:
             line["gemm_ceiling_tflops_same_run"] = gemm
         if not args.no_cpu_baseline:
