@@ -11,10 +11,21 @@
 //                                  rescales O when a row's reference max moves
 //   warps 4-7   softmax, stage 1
 //   warps 8-11  epilogue: O / l to 16 bits, staged in smem, stored by TMA
+//               (in the correction-warpgroup form, kCorrWG, they also rescale
+//               O for the tiles the softmax warps hand over)
 //   warp  12    tcgen05.mma issue (whole warp, one elected lane) + TMEM alloc
 //   warp  13    TMA producer (one thread) and item scheduler: claims items,
-//               loads each item's Q and then its K/V tiles into a ring
+//               loads each item's Q and then its K/V tiles into a ring; when
+//               it runs out of items it lets the next grid on the stream
+//               start (programmatic dependent launch)
 //   warps 14-15 idle (they complete the fourth warpgroup)
+// setmaxnreg gives the softmax warpgroups 176 registers per thread, the
+// epilogue 72 and the MMA / producer warpgroup 88.
+//
+// Launched to overlap the previous grid (PrefillParams::overlap_prev), every
+// thread that writes global memory (LSE by the softmax warps, O and the
+// split partials by the epilogue warps) first waits for that grid; reads of
+// Q, K and V start at once.
 //
 // Tensor memory (512 columns x 128 lanes): S_s = Q_s K^T at columns s*128
 // (fp32), O_s at 256 + s*D (fp32).  Softmax writes P_s as packed 16-bit

@@ -17,10 +17,13 @@
 // scheduling are those of the single-CTA kernel in fa_prefill.cuh (whose
 // helpers this file uses).
 //
-// Roles per CTA (16 warps): softmax 0-7 (stage = warp / 4), epilogue 8-11,
-// warp 12 allocates tensor memory for the pair and, in the leader only,
-// issues every MMA, warp 13 loads this CTA's operands (in the leader it also
-// claims items and publishes them to both CTAs).  Barriers the MMA waits on
+// Roles per CTA (16 warps): softmax 0-7 (stage = warp / 4), epilogue 8-11
+// (also the correction warps in the kCorrWG form), warp 12 allocates tensor
+// memory for the pair and, in the leader only, issues every MMA, warp 13
+// loads this CTA's operands (in the leader it also claims items and
+// publishes them to both CTAs; each CTA lets the next grid on the stream
+// start once it has no item left, and with overlap_prev waits for the
+// previous grid before its first global write, as fa_prefill_kernel does).  Barriers the MMA waits on
 // live in the leader and count arrivals from both CTAs; the MMA's commits
 // arrive in both CTAs (multicast); the follower's loads signal the leader's
 // barriers.

@@ -42,6 +42,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -161,16 +162,22 @@ def load_peaks():
 _HOST_ONLY = {"fa_api.cu", "fa_noalloc.cu", "fa_host.h", "fa_diag.cu"}
 
 
+_COMMENT = re.compile(r"//[^\n]*|/\*.*?\*/", re.S)
+
+
 def kernel_fingerprint() -> str:
     """sha256 (16 hex digits) of the device code and launch wrappers under
-    attention_forward_gb300/csrc: every file but the host-side dispatch."""
+    attention_forward_gb300/csrc: every file but the host-side dispatch,
+    with comments removed and white space collapsed (an edit of a comment
+    or of the layout changes no kernel)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "attention_forward_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name in _HOST_ONLY:
             continue
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            code = " ".join(_COMMENT.sub(" ", f.read()).split())
+        h.update(name.encode() + code.encode())
     return h.hexdigest()[:16]
 
 

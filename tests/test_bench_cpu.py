@@ -93,7 +93,9 @@ def test_kernel_fingerprint_covers_device_code_only(tmp_path, monkeypatch):
     api.write_text(api.read_text() + "\n// a host-side edit\n")
     assert bench.kernel_fingerprint() == f0
     dev = dst / "fa_prefill_pair.cuh"
-    dev.write_text(dev.read_text() + "\n// a device-side edit\n")
+    dev.write_text(dev.read_text() + "\n// a comment changes no kernel\n")
+    assert bench.kernel_fingerprint() == f0
+    dev.write_text(dev.read_text() + "\nconstexpr int kDeviceSideEdit = 1;\n")
     assert bench.kernel_fingerprint() != f0
 
 
