@@ -48,6 +48,7 @@
  * more than 4096 prefill calls apart must not overlap.
  * fa_get_device_status synchronises and cannot be captured;
  * fa_fwd_decode_static's scratch makes overlapping replays race.
+ * FA_FLAG_OVERLAP_PREVIOUS has been tested on streams, not inside captures.
  *
  * Device reset: the library keeps, per device, the addresses of its static
  * device arrays and its workspaces.  After cudaDeviceReset (a new primary
@@ -109,15 +110,20 @@ typedef enum {
                                         row's max moves (the softmax warps
                                         hand it those tiles) instead of the
                                         softmax warps doing it themselves;
-                                        same results, bitwise.  Ignored with
-                                        split keys                          */
+                                        same results, bitwise (measured 5-17 %
+                                        slower on GB300; kept for
+                                        comparison).  Ignored with split
+                                        keys                                */
 #define FA_FLAG_PAIR64 0x40u         /* prefill, D = 128, without a key
                                         split: CTA pairs with score tiles of
                                         64 keys and two score buffers per
                                         stage, so that the next tile's
                                         scores are computed while the
-                                        softmax of this one runs; ignored
-                                        where FA_FLAG_PAIR would be         */
+                                        softmax of this one runs (measured
+                                        slower than the default 128-key
+                                        pairs on GB300; kept for
+                                        comparison); ignored where
+                                        FA_FLAG_PAIR would be               */
 #define FA_FLAG_OVERLAP_PREVIOUS 0x80u /* prefill: launch so that the kernel
                                         may start while the previous grid on
                                         `stream` is still running (CUDA
