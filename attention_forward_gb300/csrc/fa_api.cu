@@ -88,6 +88,12 @@ struct DeviceState {
     cudaStream_t stream;
     void* ptr;
     size_t bytes;
+    // the pair kernel's tail-split arrival counters: a block of their own
+    // (no other call writes it), zeroed when made, and the epoch of the
+    // last launch that used them on this stream
+    unsigned long long* tail_ctr = nullptr;
+    size_t tail_ctr_n = 0;
+    unsigned tail_epoch = 0;
   };
   std::vector<StreamWorkspace> workspaces;
 };
@@ -225,6 +231,38 @@ fa_status_t stream_workspace(DeviceState& d, cudaStream_t stream, size_t need, v
   return FA_OK;
 }
 
+// The tail split's memory for `stream`: its partials in the stream's
+// workspace (grown to `part_bytes`) and `n_ctr` arrival counters, with the
+// launch's epoch.  A new counter block is zeroed on the stream and its
+// epochs start again at 1.
+fa_status_t stream_tail_state(DeviceState& d, cudaStream_t stream, size_t part_bytes,
+                              size_t n_ctr, void** part, unsigned long long** ctr,
+                              unsigned* epoch) {
+  fa_status_t st = stream_workspace(d, stream, part_bytes, part);
+  if (st != FA_OK) return st;
+  std::lock_guard<std::mutex> lock(g_mu);
+  for (auto& w : d.workspaces) {
+    if (w.stream != stream) continue;
+    if (w.tail_ctr_n < n_ctr) {
+      if (w.tail_ctr) cudaFree(w.tail_ctr);  // waits for the work that used it
+      w.tail_ctr = nullptr;
+      w.tail_ctr_n = 0;
+      void* p = nullptr;
+      if (cudaMalloc(&p, n_ctr * sizeof(unsigned long long)) != cudaSuccess) return FA_ERR_CUDA;
+      w.tail_ctr = static_cast<unsigned long long*>(p);
+      w.tail_ctr_n = n_ctr;
+      if (cudaMemsetAsync(p, 0, n_ctr * sizeof(unsigned long long), stream) != cudaSuccess)
+        return FA_ERR_CUDA;
+      w.tail_epoch = 0;
+    }
+    if (++w.tail_epoch == 0) w.tail_epoch = 1;
+    *ctr = w.tail_ctr;
+    *epoch = w.tail_epoch;
+    return FA_OK;
+  }
+  return FA_ERR_CUDA;  // stream_workspace made the entry
+}
+
 // Prefill key splits: only when the (query tile, head) items are fewer than
 // the SMs.  Picks the split count with the smallest estimated time, counted
 // in key tiles: rounds of one item per SM times the tiles of a range, plus
@@ -269,38 +307,68 @@ bool pair_by_default(int BH, int Sq, int Skv, int causal, int sm_count) {
   return causal ? Sq >= 8192 : (Sq >= 1024 && Skv >= 1024);
 }
 
+// The CTA-pair kernel's tail split: the pair items of a partly idle last
+// round whose key quarters, run as items of their own, fit in at most three
+// quarter-rounds (the last round then takes at most three quarters of an
+// item's time).  Non-causal only (causal launches run heaviest first and end
+// on their lightest items), at least one full round and four key tiles.
+int pair_tail_items(long long n_items, long long n_pairs, int causal, int Skv) {
+  if (causal || n_pairs <= 0 || n_items <= n_pairs) return 0;
+  if ((Skv + fa::kBN - 1) / fa::kBN < 4) return 0;
+  const long long rem = n_items % n_pairs;
+  if (rem == 0 || 4 * rem > 3 * n_pairs) return 0;
+  return static_cast<int>(rem);
+}
+
+// fa_fwd's tail-split memory for `tail` items: fp32 O / l and LSE of every
+// quarter's 512 rows, and 16 arrival counters (2 stages x 2 CTAs x 4 warps)
+// per item.
+size_t tail_part_o_bytes(int tail) {
+  return ((static_cast<size_t>(tail) * 4 * 512 * 128 * sizeof(float) + 255) / 256) * 256;
+}
+size_t tail_part_bytes(int tail) {
+  return tail_part_o_bytes(tail) + static_cast<size_t>(tail) * 4 * 512 * sizeof(float);
+}
+
+// Pairs the pair kernel (or the 64-key one) keeps on the device at once, per
+// dtype (0: not usable); checks the kernel's registers on first use.
+fa_status_t pair_slots(DeviceState& d, bool bf16, bool k64, int* out) {
+  const int ti = bf16 ? 1 : 0;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!k64 && !d.pair_checked[ti]) {
+    int regs = 0, n = 0;
+    if (fa::prefill_pair_num_regs(bf16, &regs) != cudaSuccess) return FA_ERR_CUDA;
+    if (regs == 128 && fa::prefill_pair_max_pairs(bf16, &n) != cudaSuccess) return FA_ERR_CUDA;
+    d.pair_checked[ti] = true;
+    d.pair_slots[ti] = regs == 128 ? n : 0;
+  }
+  if (k64 && !d.pair64_checked[ti]) {
+    int regs = 0, n = 0;
+    if (fa::prefill_pair64_num_regs(bf16, &regs) != cudaSuccess) return FA_ERR_CUDA;
+    if (regs == 128 && fa::prefill_pair64_max_pairs(bf16, &n) != cudaSuccess) return FA_ERR_CUDA;
+    d.pair64_checked[ti] = true;
+    d.pair64_slots[ti] = regs == 128 ? n : 0;
+  }
+  *out = k64 ? d.pair64_slots[ti] : d.pair_slots[ti];
+  return FA_OK;
+}
+
 // Prefill by CTA pairs (FA_FLAG_PAIR, D = 128, whole key range): items of 512
 // query rows, a persistent grid of two-CTA clusters.
 fa_status_t run_prefill_pair(DeviceState& d, const void* q, const void* k, const void* v,
                              void* o, float* lse, int BH, int Sq, int Skv, float scale,
                              int causal, bool bf16, unsigned flags, bool captured,
                              cudaStream_t stream) {
-  const int ti = bf16 ? 1 : 0;
   const bool k64 = (flags & FA_FLAG_PAIR64) != 0;
-  {
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!k64 && !d.pair_checked[ti]) {
-      int regs = 0, n = 0;
-      if (fa::prefill_pair_num_regs(bf16, &regs) != cudaSuccess) return FA_ERR_CUDA;
-      if (regs == 128 && fa::prefill_pair_max_pairs(bf16, &n) != cudaSuccess) return FA_ERR_CUDA;
-      d.pair_checked[ti] = true;
-      d.pair_slots[ti] = regs == 128 ? n : 0;
-    }
-    if (k64 && !d.pair64_checked[ti]) {
-      int regs = 0, n = 0;
-      if (fa::prefill_pair64_num_regs(bf16, &regs) != cudaSuccess) return FA_ERR_CUDA;
-      if (regs == 128 && fa::prefill_pair64_max_pairs(bf16, &n) != cudaSuccess) return FA_ERR_CUDA;
-      d.pair64_checked[ti] = true;
-      d.pair64_slots[ti] = regs == 128 ? n : 0;
-    }
-    if ((k64 ? d.pair64_slots[ti] : d.pair_slots[ti]) <= 0) return FA_ERR_UNSUPPORTED;
-  }
+  int slots = 0;
+  fa_status_t st = pair_slots(d, bf16, k64, &slots);
+  if (st != FA_OK) return st;
+  if (slots <= 0) return FA_ERR_UNSUPPORTED;
   constexpr int D = 128;
   // a CTA loads half of every key tile (64 of 128 keys, or 32 of 64) and
   // half of every value tile's columns (all of its 128 or 64 keys)
   const int key_tile = k64 ? 64 : fa::kBN;
   CUtensorMap tq, tk, tv, to;
-  fa_status_t st;
   if ((st = encode_3d(&tq, q, D, Sq, BH, fa::kBM, bf16)) != FA_OK) return st;
   if ((st = encode_3d(&tk, k, D, Skv, BH, key_tile / 2, bf16)) != FA_OK) return st;
   if ((st = encode_3d(&tv, v, D, Skv, BH, key_tile, bf16)) != FA_OK) return st;
@@ -326,9 +394,25 @@ fa_status_t run_prefill_pair(DeviceState& d, const void* q, const void* k, const
   const long long n_items = static_cast<long long>(p.n_qtiles) * BH;
   if (n_items > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
   p.n_items = static_cast<int>(n_items);
+  const int n_pairs = static_cast<int>(std::min<long long>(n_items, slots));
+  // the tail split, when asked for (not in the 64-key kernel, not inside a
+  // capture: a replay may run on any stream, and the counters' epoch is the
+  // launch's)
+  const int tail = k64 || captured || !(flags & FA_FLAG_TAIL_SPLIT)
+                       ? 0 : pair_tail_items(n_items, n_pairs, causal, Skv);
+  if (tail > 0) {
+    if (n_items + 3LL * tail > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+    void* part = nullptr;
+    if ((st = stream_tail_state(d, stream, tail_part_bytes(tail), static_cast<size_t>(tail) * 16,
+                                &part, &p.tail_count, &p.tail_epoch)) != FA_OK)
+      return st;
+    p.part_o = static_cast<float*>(part);
+    p.part_lse = reinterpret_cast<float*>(static_cast<char*>(part) + tail_part_o_bytes(tail));
+    p.o = o;
+    p.tail_items = tail;
+    p.n_items = static_cast<int>(n_items + 3LL * tail);
+  }
   p.sched = sched_slot(d, captured);
-  const int n_pairs = static_cast<int>(
-      std::min<long long>(n_items, k64 ? d.pair64_slots[ti] : d.pair_slots[ti]));
   const cudaError_t e =
       k64 ? fa::launch_prefill_pair64(bf16, tq, tk, tv, to, p, n_pairs, stream)
           : fa::launch_prefill_pair(bf16, (flags & FA_FLAG_CORRECTION_WG) != 0, tq, tk, tv, to,
@@ -675,8 +759,10 @@ fa_status_t fa_release_workspaces(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return FA_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_mu);
   fa_status_t out = FA_OK;
-  for (auto& w : d->workspaces)
+  for (auto& w : d->workspaces) {
     if (cudaFree(w.ptr) != cudaSuccess) out = FA_ERR_CUDA;
+    if (w.tail_ctr && cudaFree(w.tail_ctr) != cudaSuccess) out = FA_ERR_CUDA;
+  }
   d->workspaces.clear();
   return out;
 }
@@ -709,6 +795,21 @@ int fa_prefill_uses_pairs(int B, int H, int Sq, int Skv, int D, int causal, unsi
   return pair_by_default(B * H, Sq, Skv, causal, sms) ? 1 : 0;
 }
 
-int fa_version(void) { return 10200; }
+int fa_prefill_tail_items(int B, int H, int Sq, int Skv, int D, int causal, int dtype,
+                          unsigned flags) {
+  if (fa_prefill_uses_pairs(B, H, Sq, Skv, D, causal, flags, 0) != 1) return 0;
+  if ((flags & FA_FLAG_PAIR64) || !(flags & FA_FLAG_TAIL_SPLIT) ||
+      (dtype != FA_F16 && dtype != FA_BF16))
+    return 0;
+  DeviceState* d = nullptr;
+  int slots = 0;
+  if (current_device(&d, nullptr) != FA_OK ||
+      pair_slots(*d, dtype == FA_BF16, false, &slots) != FA_OK || slots <= 0)
+    return 0;
+  const long long n_items = static_cast<long long>(B) * H * ((Sq + 511) / 512);
+  return pair_tail_items(n_items, std::min<long long>(n_items, slots), causal, Skv);
+}
+
+int fa_version(void) { return 10300; }
 
 }  // extern "C"

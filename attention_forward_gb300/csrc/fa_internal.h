@@ -52,6 +52,16 @@ struct PrefillParams {
   // launched to overlap the previous grid on the stream: every thread waits
   // for it before its first global write (reads of Q, K, V may start early)
   int overlap_prev;
+  // CTA-pair kernel, last items split by keys (non-causal): the last
+  // tail_items of the n_items - 3 * tail_items pair items run as four items
+  // each, one per quarter of the key tiles, numbered after the others.  A
+  // quarter writes its rows' fp32 O / l and LSE to part_o / part_lse; the
+  // last of the four to finish a warp's 32 rows merges them into o and lse.
+  // 0: no split.
+  int tail_items;
+  void* o;                          // [BH, Sq, D] 16-bit (the merged rows)
+  unsigned long long* tail_count;   // per (item, stage, rank, warp): epoch << 8 | arrivals
+  unsigned tail_epoch;              // this launch's epoch (never 0)
 };
 
 // Decode (Sq == 1) split-KV.

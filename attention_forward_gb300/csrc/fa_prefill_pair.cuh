@@ -27,6 +27,13 @@
 // live in the leader and count arrivals from both CTAs; the MMA's commits
 // arrive in both CTAs (multicast); the follower's loads signal the leader's
 // barriers.
+//
+// Tail split (non-causal): when the items leave the last round of pairs
+// partly idle, the host numbers the last items' key quarters as items of
+// their own, so that the last round takes a quarter of an item's time per
+// step.  A quarter's softmax warps write its rows' O / l and LSE in fp32 and
+// count themselves in; the last of the four merges the rows with LSE weights
+// (pair_tail_quarter).  Nothing waits for another quarter.
 #pragma once
 #include "fa_prefill.cuh"
 
@@ -81,7 +88,14 @@ struct PairLayout {
 
 struct PairItem {
   int bh, row0, nT0, nT1;
+  int t0 = 0;     // first key tile (a quarter of a split item)
+  int part = -1;  // >= 0: partial index of a quarter (fp32 O / l and LSE to the workspace)
+  int group = 0;  // the split item's index among the split ones
 };
+
+// Key quarters of a split item: quarter r covers key tiles
+// [r * n / 4, (r + 1) * n / 4), never empty for n >= 4.
+constexpr int kTailSplits = 4;
 
 // Key tiles a 256-row stage whose first query row is `row_first` needs.
 __device__ __forceinline__ int pair_stage_tiles(int row_first, int Sq, int Skv, int causal) {
@@ -92,9 +106,18 @@ __device__ __forceinline__ int pair_stage_tiles(int row_first, int Sq, int Skv, 
   return min(n_all, last_key / kBN + 1);
 }
 
-// Pair item idx: heaviest first under causal LPT.
+// Pair item idx: heaviest first under causal LPT; the last 4 * tail_items
+// indices are the key quarters of the last tail_items items (non-causal
+// launches only).
 __device__ __forceinline__ PairItem get_pair_item(const PrefillParams& p, int idx) {
   PairItem it;
+  int part = -1, quarter = 0;
+  const int tail_first = p.n_items - kTailSplits * p.tail_items;
+  if (p.tail_items > 0 && idx >= tail_first) {
+    part = idx - tail_first;
+    quarter = part % kTailSplits;
+    idx = tail_first + part / kTailSplits;
+  }
   int qtile;
   if (p.causal && p.lpt) {
     qtile = p.n_qtiles - 1 - idx / p.BH;
@@ -106,7 +129,154 @@ __device__ __forceinline__ PairItem get_pair_item(const PrefillParams& p, int id
   it.row0 = qtile * kPairRows;
   it.nT0 = pair_stage_tiles(it.row0, p.Sq, p.Skv, p.causal);
   it.nT1 = pair_stage_tiles(it.row0 + kPairStageRows, p.Sq, p.Skv, p.causal);
+  if (part >= 0) {  // non-causal: both stages have the same key tiles
+    const int n = it.nT1;
+    it.t0 = quarter * n / kTailSplits;
+    it.nT0 = it.nT1 = (quarter + 1) * n / kTailSplits - it.t0;
+    it.part = part;
+    it.group = part / kTailSplits;
+  }
   return it;
+}
+
+// A warp's arrival at its 32 rows of a split item: returns how many of the
+// item's quarters arrived before it (3: this warp merges).  The counter holds
+// the launch's epoch above its low byte, so a count left by an earlier launch
+// (or an aborted one) reads as zero.  The first compare-and-swap guesses the
+// value a completed previous launch leaves (its epoch, four arrivals); each
+// failure returns the value to try next and means another arrival landed, so
+// the loop ends within four rounds (-1 only as a guard).
+__device__ __forceinline__ int tail_arrive(unsigned long long* c, unsigned epoch) {
+  unsigned long long old =
+      epoch > 1u ? (static_cast<unsigned long long>(epoch - 1u) << 8) | kTailSplits : 0ull;
+#pragma unroll 1
+  for (int i = 0; i < 64; ++i) {
+    const unsigned cnt = (old >> 8) == epoch ? static_cast<unsigned>(old & 0xffull) : 0u;
+    const unsigned long long nv = (static_cast<unsigned long long>(epoch) << 8) | (cnt + 1u);
+    const unsigned long long prev = atomicCAS(c, old, nv);
+    if (prev == old) return static_cast<int>(cnt);
+    old = prev;
+  }
+  return -1;
+}
+
+// The fp32 rows of one warp (32 rows of one stage and CTA) in one quarter of
+// a split item: [item][quarter][stage][rank][warp] units of 32 x 128 floats,
+// each laid out as [column / 4][row][4] so that a warp's 16-byte accesses to
+// four columns of its 32 rows are 512 contiguous bytes.
+__device__ __forceinline__ size_t tail_unit(int group, int quarter, int s, uint32_t rank, int rq) {
+  return ((static_cast<size_t>(group * kTailSplits + quarter) * 2 + s) * 2 + rank) * 4 + rq;
+}
+
+// A softmax warp's end of a quarter item (O_s final in tensor memory): its
+// rows' O / l to the workspace in fp32 and their LSE beside them, the
+// tensor-memory read released to the MMA (O_FREE), then the arrival; the
+// quarter that arrives last merges the four quarters' rows, in quarter
+// order, into the 16-bit output and the LSE -- the key-range merge of the
+// split kernel's combine (weights exp(LSE_r - LSE)).  Returns false only if
+// the arrival failed (the status word then holds the error).
+template <bool BF16>
+__device__ __forceinline__ bool pair_tail_quarter(const PrefillParams& p, const PairItem& it,
+                                                  int s, uint32_t rank, int rq, int lane,
+                                                  int row_g, uint32_t tO, float m, float l,
+                                                  uint32_t o_free_leader) {
+  constexpr int D = 128;
+  constexpr float kLog2e = 1.4426950408889634f;
+  const int quarter = it.part - it.group * kTailSplits;
+  const size_t own = tail_unit(it.group, quarter, s, rank, rq);
+  const float inv_l = l > 0.f ? 1.f / l : 0.f;
+  float4* punit = reinterpret_cast<float4*>(p.part_o + own * 32 * D) + lane;
+#pragma unroll 1
+  for (int cc = 0; cc < D / 32; ++cc) {
+    uint32_t v[2][16];
+    tmem_ld32(tO + cc * 32, v[0], v[1]);
+    tmem_wait_ld();
+    reg_fence16(v[0]);
+    reg_fence16(v[1]);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {  // columns cc * 32 + 4 e .. + 3
+      const uint32_t* x = &v[e >> 2][(e & 3) * 4];
+      punit[(cc * 8 + e) * 32] =
+          make_float4(__uint_as_float(x[0]) * inv_l, __uint_as_float(x[1]) * inv_l,
+                      __uint_as_float(x[2]) * inv_l, __uint_as_float(x[3]) * inv_l);
+    }
+  }
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive_cluster_relaxed(o_free_leader);
+  p.part_lse[own * 32 + lane] = l > 0.f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+  __threadfence();  // this lane's partial before the arrival (release)
+  __syncwarp();
+  int before = 0;
+  if (lane == 0) {
+    const size_t ctr = ((static_cast<size_t>(it.group) * 2 + s) * 2 + rank) * 4 + rq;
+    before = tail_arrive(p.tail_count + ctr, p.tail_epoch);
+  }
+  before = __shfl_sync(0xffffffffu, before, 0);
+  if (before < 0) {
+    if (lane == 0) atomicExch(p.status, kStatusTimeout);
+    return false;
+  }
+  if (before != kTailSplits - 1) return true;
+  __threadfence();  // every other quarter's partial after the arrival (acquire)
+
+  // merge this lane's row over the quarters
+  const size_t u0 = tail_unit(it.group, 0, s, rank, rq);
+  constexpr size_t kQStride = 16;  // units from one quarter to the next
+  float ls[kTailSplits];
+  float M = -INFINITY;
+#pragma unroll
+  for (int q = 0; q < kTailSplits; ++q) {
+    ls[q] = __ldcg(p.part_lse + (u0 + q * kQStride) * 32 + lane);
+    M = fmaxf(M, ls[q]);
+  }
+  const float M_use = M == -INFINITY ? 0.f : M;
+  float w[kTailSplits];
+  float W = 0.f;
+#pragma unroll
+  for (int q = 0; q < kTailSplits; ++q) {
+    w[q] = ex2_approx((ls[q] - M_use) * kLog2e);
+    W += w[q];
+  }
+  const float inv = W > 0.f ? 1.f / W : 0.f;
+  const bool row_ok = row_g < p.Sq;
+  if (row_ok) p.lse[static_cast<size_t>(it.bh) * p.Sq + row_g] = W > 0.f ? M + logf(W) : -INFINITY;
+  uint4* orow = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.o) +
+                                         (static_cast<size_t>(it.bh) * p.Sq + row_g) * D * 2);
+  const float4* src = reinterpret_cast<const float4*>(p.part_o + u0 * 32 * D) + lane;
+#pragma unroll 1
+  for (int cc = 0; cc < D / 32; ++cc) {
+    float4 a[kTailSplits][8];
+#pragma unroll
+    for (int q = 0; q < kTailSplits; ++q)
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        a[q][e] = __ldcg(src + (q * kQStride * 32 * D) / 4 + (cc * 8 + e) * 32);
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {  // 8 columns: one 16-byte store
+      float o[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = 0.f;
+#pragma unroll
+      for (int q = 0; q < kTailSplits; ++q) {
+        const float4 x = a[q][2 * h], y = a[q][2 * h + 1];
+        o[0] = fmaf(w[q], x.x, o[0]);
+        o[1] = fmaf(w[q], x.y, o[1]);
+        o[2] = fmaf(w[q], x.z, o[2]);
+        o[3] = fmaf(w[q], x.w, o[3]);
+        o[4] = fmaf(w[q], y.x, o[4]);
+        o[5] = fmaf(w[q], y.y, o[5]);
+        o[6] = fmaf(w[q], y.z, o[6]);
+        o[7] = fmaf(w[q], y.w, o[7]);
+      }
+      if (row_ok)
+        orow[cc * 4 + h] = make_uint4(pack2<BF16>(o[0] * inv, o[1] * inv),
+                                      pack2<BF16>(o[2] * inv, o[3] * inv),
+                                      pack2<BF16>(o[4] * inv, o[5] * inv),
+                                      pack2<BF16>(o[6] * inv, o[7] * inv));
+    }
+  }
+  return true;
 }
 
 // Waits on barriers that another CTA's release-arrive completes (acquire at
@@ -291,8 +461,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         // this CTA's rows; the pair's stage may reach one tile further than
         // they need (masked)
-        const bool defer = softmax_tile<D, BF16, false, kCorrWG>(tS, tO, j * kBN, stage_row0,
-                                                                 row_g, p, j > 0, m, l);
+        const bool defer = softmax_tile<D, BF16, false, kCorrWG>(
+            tS, tO, (it.t0 + j) * kBN, stage_row0, row_g, p, j > 0, m, l);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
@@ -307,6 +477,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (dep_wait) {
         grid_dependency_wait();
         dep_wait = false;
+      }
+      if (it.part >= 0) {
+        // a key quarter (nT >= 1): this warp writes its rows' partial and
+        // perhaps merges; the epilogue only counts the item
+        if (!wait_bar_warp(bar(L::O_READY + s), (n_s - 1) & 1, ctl)) { ok = false; break; }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(L::ML_FULL + s));
+        tc_fence_after();
+        if (!pair_tail_quarter<BF16>(p, it, s, rank, rq, lane, row_g, tO, m, l,
+                                     bar_l(L::O_FREE + s))) {
+          *abort_flag = 1u;
+          ok = false;
+          break;
+        }
+        continue;
       }
       if (row_g < p.Sq) {
         const float lse = l > 0.f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
@@ -390,6 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           n_t += static_cast<uint32_t>(nT);
           if (!epi_wait(bar(L::ML_FULL + s), n_e & 1)) { ok = false; continue; }
           ++n_e;
+          if (it.part >= 0) continue;  // a key quarter: its softmax warps write the rows
           inv_l = inv_l_smem[s * kBM + r];
           if (!wait_bar_warp<kSleepEpilogueNs>(bar(L::O_READY + s), (n_t - 1) & 1, ctl)) { ok = false; continue; }
           tc_fence_after();
@@ -606,10 +792,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int box = 0; box < D / 64; ++box)
             tma_load_3d_pair(dst + static_cast<uint32_t>(box * L::kKBox), &tmK,
                              bar_l(L::KV_FULL + slot), box * 64,
-                             j * kBN + static_cast<int>(rank) * 64, it.bh);
+                             (it.t0 + j) * kBN + static_cast<int>(rank) * 64, it.bh);
         } else {        // columns 64*rank .. of tile j, all 128 keys
           tma_load_3d_pair(dst, &tmV, bar_l(L::KV_FULL + slot), static_cast<int>(rank) * 64,
-                           j * kBN, it.bh);
+                           (it.t0 + j) * kBN, it.bh);
         }
         last_fill[slot] = fill;
         ++fill;

@@ -28,6 +28,7 @@ FA_FLAG_CORRECTION_WG = 0x20
 FA_FLAG_PAIR64 = 0x40
 FA_FLAG_OVERLAP_PREVIOUS = 0x80
 FA_FLAG_TEST_STALL = 0x100
+FA_FLAG_TAIL_SPLIT = 0x200
 
 _DTYPE = {torch.float16: FA_F16, torch.bfloat16: FA_BF16}
 
@@ -88,6 +89,8 @@ def load_path(path: str) -> ctypes.CDLL:
     L.fa_prefill_uses_pairs.restype = ci
     L.fa_ex2_approx.argtypes = [vp, vp, ci, vp]
     L.fa_ex2_approx.restype = ci
+    L.fa_prefill_tail_items.argtypes = [ci, ci, ci, ci, ci, ci, ci, ctypes.c_uint]
+    L.fa_prefill_tail_items.restype = ci
     L.fa_version.argtypes = []
     L.fa_version.restype = ci
     return L
@@ -240,6 +243,14 @@ def fa_prefill_uses_pairs(B: int, H: int, Sq: int, Skv: int, D: int, causal: boo
                           flags: int = 0, num_splits: int = 0) -> bool:
     return bool(load().fa_prefill_uses_pairs(B, H, Sq, Skv, D, int(bool(causal)), flags,
                                               num_splits))
+
+
+def fa_prefill_tail_items(B: int, H: int, Sq: int, Skv: int, D: int, causal: bool,
+                          dtype=torch.bfloat16, flags: int = 0) -> int:
+    """Pair items that fa_fwd_ex with these arguments splits into key
+    quarters (FA_FLAG_TAIL_SPLIT); 0 if none."""
+    return int(load().fa_prefill_tail_items(B, H, Sq, Skv, D, int(bool(causal)),
+                                             _DTYPE[dtype], flags))
 
 
 def fa_ex2_approx(x, stream=None):

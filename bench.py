@@ -493,6 +493,11 @@ def roofline(fa, w, launch_s, kflags):
     peak = float(peaks["bf16_tflops"])
     pairs = fa.fa_prefill_uses_pairs(w.B, w.H, w.Sq, w.Skv, w.D, w.causal, kflags)
     kern = "fa_prefill_pair_kernel (two-CTA clusters)" if pairs else "fa_prefill_kernel"
+    if pairs:
+        tail = fa.fa_prefill_tail_items(w.B, w.H, w.Sq, w.Skv, w.D, w.causal,
+                                        inputs.DTYPES[w.dtype], kflags)
+        if tail:
+            kern += f", its last {tail} items split into key quarters (merged in the kernel)"
     if launches_per_step(fa, w) > 1 and not pairs:
         kern += " with split keys + fa_decode_combine_kernel (one step)"
     return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",

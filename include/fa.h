@@ -40,8 +40,9 @@
  * CUDA graphs: fa_fwd, fa_fwd_ex and fa_fwd_host may be called while
  * `stream` is being captured; the graph then replays the same launches, on
  * any stream.  A captured call uses no library-owned workspace, so the
- * shapes fa_fwd would split (few query tiles, or decode) run unsplit there;
- * fa_fwd_ex with a caller workspace keeps the split, and the workspace is
+ * shapes fa_fwd would split (few query tiles, or decode) run unsplit there,
+ * and FA_FLAG_TAIL_SPLIT is ignored;
+ * fa_fwd_ex with a caller workspace keeps the key split, and the workspace is
  * then the graph's to keep.  Each captured prefill takes one of 4096
  * scheduler slots reserved for captures, which direct launches never use:
  * replays of one graph run in stream order, and replays of graphs captured
@@ -144,6 +145,11 @@ typedef enum {
                                         K tile, so the consumers' bounded
                                         waits run out and the kernel reports
                                         FA_ERR_TIMEOUT                      */
+#define FA_FLAG_TAIL_SPLIT 0x200u    /* CTA pairs, non-causal: the tail
+                                        split (see fa_fwd).  Measured slower
+                                        than without it on GB300 (0.94 on
+                                        the B4 H16 S4096 workload); kept
+                                        for comparison                      */
 
 /*
  * fa_fwd -- the whole forward pass for one batch, on `stream`.
@@ -156,7 +162,17 @@ typedef enum {
  * be fewer than 1024 calls apart.  When the (256-row query tile, head)
  * items are fewer than the SMs (short query blocks, few heads), the keys of
  * each item are split into ranges whose fp32 partials a combine kernel
- * merges.  Decode (Sq == 1): split-KV kernel plus combine kernel.  The
+ * merges.  Decode (Sq == 1): split-KV kernel plus combine kernel.
+ * Tail split (FA_FLAG_TAIL_SPLIT, fa_fwd_ex only): when the CTA-pair
+ * kernel's 512-row items (non-causal, at least 4 key tiles) leave its last
+ * round of pairs partly idle, and the quarters of those last items fit in
+ * at most three quarter-rounds, each of the last items runs as four items
+ * over a quarter of the key tiles; the quarter that finishes last merges
+ * their fp32 partials inside the kernel (the key-split merge: weights
+ * exp(LSE_r - LSE)), so the rows of those items differ from an unsplit run
+ * by rounding only.  Outside a CUDA graph capture, the partials (1 MiB per
+ * split item) and arrival counters go to the library's workspace for the
+ * stream, as fa_fwd's key splits do.  The
  * partials go to a workspace that the library allocates on the first call
  * that needs one, one per (device, stream handle), and keeps until
  * fa_release_workspaces() or process exit (use fa_fwd_ex to supply your
@@ -292,6 +308,13 @@ const char *fa_status_string(fa_status_t status);
  * would reject).  Reads the current device's SM count; launches nothing. */
 int fa_prefill_uses_pairs(int B, int H, int Sq, int Skv, int D, int causal,
                           unsigned flags, int num_splits);
+
+/* Number of 512-row CTA-pair items that fa_fwd_ex with these arguments
+ * (outside a capture) splits into key quarters (FA_FLAG_TAIL_SPLIT: see
+ * fa_fwd); 0 when there is none.  Reads the current device's SM count
+ * and the pair kernel's occupancy; launches nothing. */
+int fa_prefill_tail_items(int B, int H, int Sq, int Skv, int D, int causal,
+                          int dtype, unsigned flags);
 
 /* Library ABI version: major * 10000 + minor * 100 + patch. */
 int fa_version(void);

@@ -31,7 +31,7 @@ def test_header_declares_the_boundary():
               "fa_host_staging_bytes", "fa_get_device_status",
               "fa_set_watchdog_ns", "fa_status_string", "fa_version",
               "fa_prefill_uses_pairs", "fa_release_workspaces",
-              "fa_fwd_decode_static"):
+              "fa_fwd_decode_static", "fa_prefill_tail_items"):
         assert n in names, n
 
 
@@ -45,7 +45,7 @@ def test_status_strings_and_version(lib):
     for st in range(6):
         assert fa.fa_status_string(st)
     assert fa.fa_status_string(99) == "unknown status"
-    assert fa.fa_version() == 10200
+    assert fa.fa_version() == 10300
 
 
 def test_pair_selection_without_a_gpu(lib):
@@ -68,6 +68,9 @@ def test_pair_selection_without_a_gpu(lib):
     assert fa.fa_prefill_uses_pairs(2, 16, 8192, 8192, 128, True)
     assert fa.fa_prefill_uses_pairs(1, 16, 16384, 16384, 128, True)
     assert not fa.fa_prefill_uses_pairs(1, 1, 4096, 4096, 128, False)  # 8 items
+    # the tail split needs the device's pair occupancy: none without a GPU
+    assert fa.fa_prefill_tail_items(4, 16, 4096, 4096, 128, False,
+                                    flags=fa.FA_FLAG_TAIL_SPLIT) == 0
 
 
 def _call(lib, q=16, k=16, v=16, o=16, lse=16, B=1, H=1, Sq=8, Skv=8, D=64,
