@@ -25,7 +25,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-Xptxas", "-v", "--expt-relaxed-constexpr",
                      f"-I{os.path.join(ROOT, 'include')}"]
-SOURCES = ["fa_prefill_d128.cu", "fa_prefill_d64.cu", "fa_prefill_pair.cu",
+SOURCES = ["fa_prefill_d128.cu", "fa_prefill_d64.cu", "fa_prefill_d64x3.cu", "fa_prefill_pair.cu",
            "fa_decode.cu", "fa_api.cu", "fa_noalloc.cu", "fa_diag.cu"]
 
 

@@ -82,6 +82,8 @@ struct DeviceState {
   int pair_slots[2] = {};  // 0: not usable
   bool pair64_checked[2] = {};
   int pair64_slots[2] = {};  // the 64-key pair kernel; 0: not usable
+  bool d64x3_checked[2] = {};
+  bool d64x3_ok[2] = {};     // the three-stage D = 64 kernel, per dtype
   // fa_fwd's workspaces for split partials, one per stream handle (calls on
   // one stream run in order; calls on different streams may overlap)
   struct StreamWorkspace {
@@ -421,6 +423,57 @@ fa_status_t run_prefill_pair(DeviceState& d, const void* q, const void* k, const
   return FA_OK;
 }
 
+// Prefill at D = 64 by the three-stage kernel (FA_FLAG_D64_THREE_STAGE): items
+// of 384 query rows, 96-key tiles, one persistent CTA per SM.
+fa_status_t run_prefill_d64x3(DeviceState& d, const void* q, const void* k, const void* v,
+                              void* o, float* lse, int BH, int Sq, int Skv, float scale,
+                              int causal, bool bf16, unsigned flags, bool captured,
+                              cudaStream_t stream) {
+  const int ti = bf16 ? 1 : 0;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!d.d64x3_checked[ti]) {
+      int regs = 0;
+      if (fa::prefill_d64x3_num_regs(bf16, &regs) != cudaSuccess) return FA_ERR_CUDA;
+      d.d64x3_checked[ti] = true;
+      d.d64x3_ok[ti] = regs == 128;
+    }
+    if (!d.d64x3_ok[ti]) return FA_ERR_UNSUPPORTED;
+  }
+  constexpr int D = 64;
+  CUtensorMap tq, tk, tv, to;
+  fa_status_t st;
+  if ((st = encode_3d(&tq, q, D, Sq, BH, fa::kBM, bf16)) != FA_OK) return st;
+  if ((st = encode_3d(&tk, k, D, Skv, BH, fa::kN3, bf16)) != FA_OK) return st;
+  if ((st = encode_3d(&tv, v, D, Skv, BH, fa::kN3, bf16)) != FA_OK) return st;
+  if ((st = encode_3d(&to, o, D, Sq, BH, 32, bf16)) != FA_OK) return st;
+  fa::PrefillParams p{};
+  p.lse = lse;
+  p.status = d.status;
+  p.timeout_ns = g_watchdog_ns.load();
+  p.BH = BH;
+  p.Sq = Sq;
+  p.Skv = Skv;
+  p.n_qtiles = (Sq + fa::kRows3 - 1) / fa::kRows3;
+  p.causal = causal ? 1 : 0;
+  p.lpt = (flags & FA_FLAG_NO_LPT) ? 0 : 1;
+  p.always_rescale = (flags & FA_FLAG_ALWAYS_RESCALE) ? 1 : 0;
+  p.test_stall = (flags & FA_FLAG_TEST_STALL) ? 1 : 0;
+  p.overlap_prev = (flags & FA_FLAG_OVERLAP_PREVIOUS) ? 1 : 0;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.rescale_tau = (flags & FA_FLAG_EXACT_MAX) ? 0.f : 8.f;
+  p.n_splits = 1;
+  p.tiles_per_split = (Skv + fa::kN3 - 1) / fa::kN3;
+  const long long n_items = static_cast<long long>(p.n_qtiles) * BH;
+  if (n_items > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  p.n_items = static_cast<int>(n_items);
+  p.sched = sched_slot(d, captured);
+  const int grid = static_cast<int>(std::min<long long>(n_items, d.sm_count > 0 ? d.sm_count : 1));
+  if (fa::launch_prefill_d64x3(bf16, tq, tk, tv, to, p, grid, stream) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return FA_OK;
+}
+
 fa_status_t run_prefill(DeviceState& d, const void* q, const void* k, const void* v,
                         void* o, float* lse, int B, int H, int Sq, int Skv, int D,
                         float scale, int causal, bool bf16, unsigned flags,
@@ -468,6 +521,10 @@ fa_status_t run_prefill(DeviceState& d, const void* q, const void* k, const void
   p.rescale_tau = (flags & FA_FLAG_EXACT_MAX) ? 0.f : 8.f;
   const int n_tiles = (Skv + fa::kBN - 1) / fa::kBN;
   int n_splits = prefill_splits(BH, Sq, Skv, d.sm_count, num_splits);
+  if (D == 64 && (flags & FA_FLAG_D64_THREE_STAGE) && n_splits == 1 &&
+      !(flags & FA_FLAG_CORRECTION_WG))
+    return run_prefill_d64x3(d, q, k, v, o, lse, BH, Sq, Skv, scale, causal, bf16, flags,
+                             captured, stream);
   if (n_splits > 1 && static_cast<long long>(BH) * Sq > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
   p.tiles_per_split = (n_tiles + n_splits - 1) / n_splits;
   n_splits = (n_tiles + p.tiles_per_split - 1) / p.tiles_per_split;

@@ -18,6 +18,11 @@ constexpr int kBN = 128;
 constexpr int kStages = 2;
 constexpr int kRowsPerCta = kBM * kStages;
 constexpr int kThreads = 512;  // 4 warpgroups
+// The three-stage D = 64 kernel: three stages of kBM rows per item, key
+// tiles of kN3.
+constexpr int kN3 = 96;
+constexpr int kStages3 = 3;
+constexpr int kRows3 = kStages3 * kBM;
 
 // Dynamic item scheduler: slots of a static device array, one per launch
 // (chosen round-robin by the host), two words each: [0] = items claimed,

@@ -33,6 +33,13 @@ cudaError_t launch_prefill_pair64(bool bf16, const CUtensorMap& q, const CUtenso
                                   const CUtensorMap& v, const CUtensorMap& o,
                                   const PrefillParams& p, int n_pairs, cudaStream_t stream);
 
+// The three-stage prefill kernel for D = 64 (whole key range; 96-key tiles,
+// 384-row items): registers per thread and the launch.
+cudaError_t prefill_d64x3_num_regs(bool bf16, int* regs);
+cudaError_t launch_prefill_d64x3(bool bf16, const CUtensorMap& q, const CUtensorMap& k,
+                                 const CUtensorMap& v, const CUtensorMap& o,
+                                 const PrefillParams& p, int grid, cudaStream_t stream);
+
 int decode_smem_bytes(int D);
 cudaError_t launch_decode(int D, bool bf16, const DecodeParams& p, int grid,
                           cudaStream_t stream);

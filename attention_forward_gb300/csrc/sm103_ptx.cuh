@@ -332,6 +332,35 @@ __device__ __forceinline__ void umma_f16_ts_k128(uint32_t d_tmem, uint32_t a_tme
       : "memory");
 }
 
+// Six K=16 steps of D (+)= A * B for a K = 96 contraction: A (128 rows x 96
+// K of 16-bit pairs) in tensor memory, 8 columns per step; B MN-major
+// 128-byte swizzled in shared memory, 16 K rows (2048 bytes = 128
+// descriptor units) per step.
+__device__ __forceinline__ void umma_f16_ts_k96(uint32_t d_tmem, uint32_t a_tmem,
+                                                uint64_t b_desc, uint32_t idesc,
+                                                uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e, t;\n\t"
+      ".reg .b32 a1, a2, a3, a4, a5;\n\t"
+      ".reg .b64 b1, b2, b3, b4, b5;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 t, 0, 0;\n\t"
+      "add.s32 a1, %1, 8;\n\t  add.s64 b1, %2, 128;\n\t"
+      "add.s32 a2, %1, 16;\n\t add.s64 b2, %2, 256;\n\t"
+      "add.s32 a3, %1, 24;\n\t add.s64 b3, %2, 384;\n\t"
+      "add.s32 a4, %1, 32;\n\t add.s64 b4, %2, 512;\n\t"
+      "add.s32 a5, %1, 40;\n\t add.s64 b5, %2, 640;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a4], b4, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a5], b5, %3, t;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 op issued so far by the elected
 // lane has completed (the same lane elect.sync picks for the MMAs).
 __device__ __forceinline__ void umma_commit(uint32_t bar) {

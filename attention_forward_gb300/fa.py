@@ -29,6 +29,7 @@ FA_FLAG_PAIR64 = 0x40
 FA_FLAG_OVERLAP_PREVIOUS = 0x80
 FA_FLAG_TEST_STALL = 0x100
 FA_FLAG_TAIL_SPLIT = 0x200
+FA_FLAG_D64_THREE_STAGE = 0x400
 
 _DTYPE = {torch.float16: FA_F16, torch.bfloat16: FA_BF16}
 

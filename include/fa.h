@@ -145,6 +145,12 @@ typedef enum {
                                         K tile, so the consumers' bounded
                                         waits run out and the kernel reports
                                         FA_ERR_TIMEOUT                      */
+#define FA_FLAG_D64_THREE_STAGE 0x400u /* prefill, D = 64, without a key
+                                        split and without
+                                        FA_FLAG_CORRECTION_WG: the
+                                        three-stage kernel (384-row items of
+                                        three 128-row stages, 96-key tiles);
+                                        ignored otherwise                   */
 #define FA_FLAG_TAIL_SPLIT 0x200u    /* CTA pairs, non-causal: the tail
                                         split (see fa_fwd).  Measured slower
                                         than without it on GB300 (0.94 on
