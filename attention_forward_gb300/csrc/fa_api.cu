@@ -400,7 +400,8 @@ fa_status_t run_prefill_pair(DeviceState& d, const void* q, const void* k, const
   // the tail split, when asked for (not in the 64-key kernel, not inside a
   // capture: a replay may run on any stream, and the counters' epoch is the
   // launch's)
-  const int tail = k64 || captured || !(flags & FA_FLAG_TAIL_SPLIT)
+  const int tail = k64 || captured || !(flags & FA_FLAG_TAIL_SPLIT) ||
+                           (flags & FA_FLAG_CORRECTION_WG)
                        ? 0 : pair_tail_items(n_items, n_pairs, causal, Skv);
   if (tail > 0) {
     if (n_items + 3LL * tail > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
@@ -855,7 +856,7 @@ int fa_prefill_uses_pairs(int B, int H, int Sq, int Skv, int D, int causal, unsi
 int fa_prefill_tail_items(int B, int H, int Sq, int Skv, int D, int causal, int dtype,
                           unsigned flags) {
   if (fa_prefill_uses_pairs(B, H, Sq, Skv, D, causal, flags, 0) != 1) return 0;
-  if ((flags & FA_FLAG_PAIR64) || !(flags & FA_FLAG_TAIL_SPLIT) ||
+  if ((flags & (FA_FLAG_PAIR64 | FA_FLAG_CORRECTION_WG)) || !(flags & FA_FLAG_TAIL_SPLIT) ||
       (dtype != FA_F16 && dtype != FA_BF16))
     return 0;
   DeviceState* d = nullptr;

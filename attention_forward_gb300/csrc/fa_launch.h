@@ -18,7 +18,8 @@ cudaError_t launch_prefill(int D, bool bf16, bool corr, const CUtensorMap& q,
                            int grid, cudaStream_t stream);
 
 // CTA-pair prefill (D = 128, whole key range): registers per thread, the
-// number of two-CTA clusters that fit on the device, and the launch.
+// number of two-CTA clusters that fit on the device, and the launch (the
+// tail-split form when p.tail_items > 0, which excludes corr).
 cudaError_t prefill_pair_num_regs(bool bf16, int* regs);
 cudaError_t prefill_pair_max_pairs(bool bf16, int* n);
 cudaError_t launch_prefill_pair(bool bf16, bool corr, const CUtensorMap& q,

@@ -1,6 +1,7 @@
 // fa_prefill_pair.cu -- instantiations and launcher of the CTA-pair prefill
 // kernel (head dimension 128, fp16 and bf16, whole key range; merged or
-// correction-warpgroup form), launched with clusters of two CTAs.
+// correction-warpgroup form, and the merged form with the tail split),
+// launched with clusters of two CTAs.
 #include <mutex>
 
 #include "fa_launch.h"
@@ -10,7 +11,7 @@
 namespace fa {
 namespace {
 
-template <bool BF16, bool kCorr>
+template <bool BF16, bool kCorr, bool kTail = false>
 cudaError_t set_attrs() {
   static std::mutex mu;
   static bool done[64] = {};
@@ -20,7 +21,7 @@ cudaError_t set_attrs() {
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(mu);
   if (done[dev]) return cudaSuccess;
-  e = cudaFuncSetAttribute(fa_prefill_pair_kernel<BF16, kCorr>,
+  e = cudaFuncSetAttribute(fa_prefill_pair_kernel<BF16, kCorr, kTail>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, PairLayout::kSmemBytes);
   if (e == cudaSuccess) done[dev] = true;
   return e;
@@ -47,18 +48,18 @@ cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribut
   return cfg;
 }
 
-template <bool BF16, bool kCorr>
+template <bool BF16, bool kCorr, bool kTail = false>
 cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                    const CUtensorMap& o, const PrefillParams& p, int n_pairs,
                    cudaStream_t stream) {
-  cudaError_t e = set_attrs<BF16, kCorr>();
+  cudaError_t e = set_attrs<BF16, kCorr, kTail>();
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[2];
   const cudaLaunchConfig_t cfg = pair_config(2 * n_pairs, stream, attr, p.overlap_prev != 0);
-  return cudaLaunchKernelEx(&cfg, fa_prefill_pair_kernel<BF16, kCorr>, q, k, v, o, p);
+  return cudaLaunchKernelEx(&cfg, fa_prefill_pair_kernel<BF16, kCorr, kTail>, q, k, v, o, p);
 }
 
-// Both forms have the same shared memory and threads, so the same number of
+// Every form has the same shared memory and threads, so the same number of
 // pairs fits; the merged form is queried.
 template <bool BF16>
 cudaError_t max_pairs(int* n) {
@@ -66,20 +67,25 @@ cudaError_t max_pairs(int* n) {
   if (e != cudaSuccess) return e;
   e = set_attrs<BF16, true>();
   if (e != cudaSuccess) return e;
+  e = set_attrs<BF16, false, true>();
+  if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[2];
   const cudaLaunchConfig_t cfg = pair_config(2, nullptr, attr);
   return cudaOccupancyMaxActiveClusters(n, fa_prefill_pair_kernel<BF16, false>, &cfg);
 }
 
-// Registers per thread of both forms: their count, or the first that is not
-// 128 (the register split assumes 128).
+// Registers per thread of the three forms: their count, or the first that
+// is not 128 (the register split assumes 128).
 template <bool BF16>
 cudaError_t num_regs(int* regs) {
-  cudaFuncAttributes a{}, b{};
+  cudaFuncAttributes a{}, b{}, c{};
   cudaError_t e = cudaFuncGetAttributes(&a, fa_prefill_pair_kernel<BF16, false>);
   if (e != cudaSuccess) return e;
   e = cudaFuncGetAttributes(&b, fa_prefill_pair_kernel<BF16, true>);
-  if (e == cudaSuccess) *regs = a.numRegs != 128 ? a.numRegs : b.numRegs;
+  if (e != cudaSuccess) return e;
+  e = cudaFuncGetAttributes(&c, fa_prefill_pair_kernel<BF16, false, true>);
+  if (e == cudaSuccess)
+    *regs = a.numRegs != 128 ? a.numRegs : (b.numRegs != 128 ? b.numRegs : c.numRegs);
   return e;
 }
 
@@ -159,6 +165,9 @@ cudaError_t launch_prefill_pair(bool bf16, bool corr, const CUtensorMap& q,
                                 const CUtensorMap& k, const CUtensorMap& v,
                                 const CUtensorMap& o, const PrefillParams& p, int n_pairs,
                                 cudaStream_t stream) {
+  if (p.tail_items > 0)  // the tail split (merged form only)
+    return bf16 ? launch<true, false, true>(q, k, v, o, p, n_pairs, stream)
+                : launch<false, false, true>(q, k, v, o, p, n_pairs, stream);
   if (corr)
     return bf16 ? launch<true, true>(q, k, v, o, p, n_pairs, stream)
                 : launch<false, true>(q, k, v, o, p, n_pairs, stream);

@@ -86,12 +86,21 @@ struct PairLayout {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-struct PairItem {
+// One pair item: 512 query rows of one (batch, head) over key tiles
+// [t0, t0 + nT1).  The tail-split form also numbers the quarters.
+template <bool kTail>
+struct PairItemT {
+  int bh, row0, nT0, nT1;
+  static constexpr int t0 = 0, part = -1, group = 0;
+};
+template <>
+struct PairItemT<true> {
   int bh, row0, nT0, nT1;
   int t0 = 0;     // first key tile (a quarter of a split item)
   int part = -1;  // >= 0: partial index of a quarter (fp32 O / l and LSE to the workspace)
   int group = 0;  // the split item's index among the split ones
 };
+using PairItem = PairItemT<false>;
 
 // Key quarters of a split item: quarter r covers key tiles
 // [r * n / 4, (r + 1) * n / 4), never empty for n >= 4.
@@ -106,14 +115,15 @@ __device__ __forceinline__ int pair_stage_tiles(int row_first, int Sq, int Skv, 
   return min(n_all, last_key / kBN + 1);
 }
 
-// Pair item idx: heaviest first under causal LPT; the last 4 * tail_items
-// indices are the key quarters of the last tail_items items (non-causal
-// launches only).
-__device__ __forceinline__ PairItem get_pair_item(const PrefillParams& p, int idx) {
-  PairItem it;
+// Pair item idx: heaviest first under causal LPT; with kTail, the last
+// 4 * tail_items indices are the key quarters of the last tail_items items
+// (non-causal launches only).
+template <bool kTail>
+__device__ __forceinline__ PairItemT<kTail> get_pair_item(const PrefillParams& p, int idx) {
+  PairItemT<kTail> it;
   int part = -1, quarter = 0;
   const int tail_first = p.n_items - kTailSplits * p.tail_items;
-  if (p.tail_items > 0 && idx >= tail_first) {
+  if (kTail && p.tail_items > 0 && idx >= tail_first) {
     part = idx - tail_first;
     quarter = part % kTailSplits;
     idx = tail_first + part / kTailSplits;
@@ -129,12 +139,14 @@ __device__ __forceinline__ PairItem get_pair_item(const PrefillParams& p, int id
   it.row0 = qtile * kPairRows;
   it.nT0 = pair_stage_tiles(it.row0, p.Sq, p.Skv, p.causal);
   it.nT1 = pair_stage_tiles(it.row0 + kPairStageRows, p.Sq, p.Skv, p.causal);
-  if (part >= 0) {  // non-causal: both stages have the same key tiles
-    const int n = it.nT1;
-    it.t0 = quarter * n / kTailSplits;
-    it.nT0 = it.nT1 = (quarter + 1) * n / kTailSplits - it.t0;
-    it.part = part;
-    it.group = part / kTailSplits;
+  if constexpr (kTail) {
+    if (part >= 0) {  // non-causal: both stages have the same key tiles
+      const int n = it.nT1;
+      it.t0 = quarter * n / kTailSplits;
+      it.nT0 = it.nT1 = (quarter + 1) * n / kTailSplits - it.t0;
+      it.part = part;
+      it.group = part / kTailSplits;
+    }
   }
   return it;
 }
@@ -176,7 +188,8 @@ __device__ __forceinline__ size_t tail_unit(int group, int quarter, int s, uint3
 // split kernel's combine (weights exp(LSE_r - LSE)).  Returns false only if
 // the arrival failed (the status word then holds the error).
 template <bool BF16>
-__device__ __forceinline__ bool pair_tail_quarter(const PrefillParams& p, const PairItem& it,
+__device__ __forceinline__ bool pair_tail_quarter(const PrefillParams& p,
+                                                  const PairItemT<true>& it,
                                                   int s, uint32_t rank, int rq, int lane,
                                                   int row_g, uint32_t tO, float m, float l,
                                                   uint32_t o_free_leader) {
@@ -346,8 +359,9 @@ constexpr unsigned kPairSleepEpilogueNs = 257;
 // kCorrWG: the correction-warpgroup form, as in fa_prefill_kernel: a softmax
 // warp whose rows moved their reference max hands the tile to the epilogue
 // warp of its lane quarter (same CTA), which rescales O and makes the tile's
-// PV_READY arrival on the leader in its place.
-template <bool BF16, bool kCorrWG = false>
+// PV_READY arrival on the leader in its place.  kTail: the tail split (an
+// instantiation of its own, so that the other forms carry none of its code).
+template <bool BF16, bool kCorrWG = false, bool kTail = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ,
                            const __grid_constant__ CUtensorMap tmK,  // box: 64 keys
@@ -355,6 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                            const __grid_constant__ CUtensorMap tmO,
                            const PrefillParams p) {
   using L = PairLayout;
+  using Item = PairItemT<kTail>;
   constexpr int D = L::D;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -448,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int idx = pair_take_item<kPairSleepSoftmaxNs>(item_ring, bar(L::ITEM_FULL),
                                                           bar_l(L::ITEM_EMPTY), k, ctl, ok);
       if (!ok || idx < 0) break;
-      const PairItem it = get_pair_item(p, idx);
+      const Item it = get_pair_item<kTail>(p, idx);
       const int nT = s == 0 ? it.nT0 : it.nT1;
       const int stage_row0 = it.row0 + s * kPairStageRows + static_cast<int>(rank) * kBM;
       const int row_g = stage_row0 + r;
@@ -478,20 +493,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         grid_dependency_wait();
         dep_wait = false;
       }
-      if (it.part >= 0) {
-        // a key quarter (nT >= 1): this warp writes its rows' partial and
-        // perhaps merges; the epilogue only counts the item
-        if (!wait_bar_warp(bar(L::O_READY + s), (n_s - 1) & 1, ctl)) { ok = false; break; }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(L::ML_FULL + s));
-        tc_fence_after();
-        if (!pair_tail_quarter<BF16>(p, it, s, rank, rq, lane, row_g, tO, m, l,
-                                     bar_l(L::O_FREE + s))) {
-          *abort_flag = 1u;
-          ok = false;
-          break;
+      if constexpr (kTail) {
+        if (it.part >= 0) {
+          // a key quarter (nT >= 1): this warp writes its rows' partial and
+          // perhaps merges; the epilogue only counts the item
+          if (!wait_bar_warp(bar(L::O_READY + s), (n_s - 1) & 1, ctl)) { ok = false; break; }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(L::ML_FULL + s));
+          tc_fence_after();
+          if (!pair_tail_quarter<BF16>(p, it, s, rank, rq, lane, row_g, tO, m, l,
+                                       bar_l(L::O_FREE + s))) {
+            *abort_flag = 1u;
+            ok = false;
+            break;
+          }
+          continue;
         }
-        continue;
       }
       if (row_g < p.Sq) {
         const float lse = l > 0.f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
@@ -558,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int idx = pair_take_item<kPairSleepEpilogueNs>(item_ring, bar(L::ITEM_FULL),
                                                            bar_l(L::ITEM_EMPTY), k, ctl, ok);
       if (!ok || idx < 0) break;
-      const PairItem it = get_pair_item(p, idx);
+      const Item it = get_pair_item<kTail>(p, idx);
       if (dep_wait) {
         grid_dependency_wait();
         dep_wait = false;
@@ -575,7 +592,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           n_t += static_cast<uint32_t>(nT);
           if (!epi_wait(bar(L::ML_FULL + s), n_e & 1)) { ok = false; continue; }
           ++n_e;
-          if (it.part >= 0) continue;  // a key quarter: its softmax warps write the rows
+          if constexpr (kTail)
+            if (it.part >= 0) continue;  // a key quarter: its softmax warps write the rows
           inv_l = inv_l_smem[s * kBM + r];
           if (!wait_bar_warp<kSleepEpilogueNs>(bar(L::O_READY + s), (n_t - 1) & 1, ctl)) { ok = false; continue; }
           tc_fence_after();
@@ -636,7 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                           kIdescPV, acc ? 1u : 0u);
         umma_commit_pair(bar(L::O_READY + s), kBoth);
       };
-      auto begin = [&](const PairItem& it, int kq, int f) -> bool {
+      auto begin = [&](const Item& it, int kq, int f) -> bool {
         if (!wait_bar_warp<kSleepMmaNs>(bar(L::Q_FULL + 0), kq & 1, ctl) ||
             !wait_bar_warp<kSleepMmaNs>(bar(L::Q_FULL + 1), kq & 1, ctl))
           return false;
@@ -660,20 +678,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       const int first = pair_take_item<kPairSleepMmaNs>(item_ring, bar(L::ITEM_FULL),
                                                         bar_l(L::ITEM_EMPTY), 0, ctl, ok);
-      PairItem cur = first >= 0 ? get_pair_item(p, first) : PairItem{0, 0, 0, 0};
+      Item cur = first >= 0 ? get_pair_item<kTail>(p, first) : Item{0, 0, 0, 0};
       if (ok && first >= 0) ok = begin(cur, 0, 0);
       else ok = false;
 #pragma unroll 1
       while (ok) {
         bool taken = false, has_next = false;
-        PairItem nxt{0, 0, 0, 0};
+        Item nxt{0, 0, 0, 0};
         auto take_next = [&]() {
           if (taken) return;
           taken = true;
           const int nidx = pair_take_item<kPairSleepMmaNs>(item_ring, bar(L::ITEM_FULL),
                                                            bar_l(L::ITEM_EMPTY), kq + 1, ctl, ok);
           has_next = ok && nidx >= 0;
-          if (has_next) nxt = get_pair_item(p, nidx);
+          if (has_next) nxt = get_pair_item<kTail>(p, nidx);
         };
         const int fN = fK + 2 * cur.nT1;
 #pragma unroll 1
@@ -766,7 +784,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int nq[2] = {0, 0};
       bool ok = true;
       const int qrow_off = static_cast<int>(rank) * kBM;
-      auto load_q = [&](const PairItem& it, int s) -> bool {
+      auto load_q = [&](const Item& it, int s) -> bool {
         if (nq[s] > 0 && !wait_bar<kSleepProducerNs>(bar(L::Q_EMPTY + s), (nq[s] - 1) & 1, ctl)) return false;
         if (leader) mbar_arrive_expect_tx(bar(L::Q_FULL + s), 2 * L::kQBytes);
 #pragma unroll
@@ -777,7 +795,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++nq[s];
         return true;
       };
-      auto load_kv = [&](const PairItem& it, int kv, int j) -> bool {
+      auto load_kv = [&](const Item& it, int kv, int j) -> bool {
         const int slot = fill % L::kSlots;
         const uint32_t par = static_cast<uint32_t>(((fill / L::kSlots) & 1) ^ 1);
         if (!wait_bar<kSleepProducerNs>(bar(L::KV_EMPTY + slot), par, ctl)) return false;
@@ -835,7 +853,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           grid_launch_dependents();  // the next grid may take the SMs
           break;
         }
-        const PairItem it = get_pair_item(p, idx);
+        const Item it = get_pair_item<kTail>(p, idx);
         ok = load_q(it, 0);
 #pragma unroll 1
         for (int j = 0; ok && j < it.nT1; ++j) {
@@ -852,7 +870,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the next item's Q (all 512 rows, both CTAs' shares) into L2
             // now: its loads can start only once this item's last QKs have
             // read the Q buffers
-            const PairItem nx = get_pair_item(p, idx);
+            const Item nx = get_pair_item<kTail>(p, idx);
 #pragma unroll 1
             for (int rb = 0; rb < kPairRows / kBM; ++rb)
 #pragma unroll

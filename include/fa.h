@@ -151,7 +151,8 @@ typedef enum {
                                         three-stage kernel (384-row items of
                                         three 128-row stages, 96-key tiles);
                                         ignored otherwise                   */
-#define FA_FLAG_TAIL_SPLIT 0x200u    /* CTA pairs, non-causal: the tail
+#define FA_FLAG_TAIL_SPLIT 0x200u    /* CTA pairs, non-causal, without
+                                        FA_FLAG_CORRECTION_WG: the tail
                                         split (see fa_fwd).  Measured slower
                                         than without it on GB300 (0.94 on
                                         the B4 H16 S4096 workload); kept

@@ -134,22 +134,25 @@ def test_after_an_aborted_launch():
 
 def test_selection_and_forms_agree():
     """The split needs the flag (fa_fwd never splits), pairs, a non-causal
-    mask and the 128-key kernel; the correction-warpgroup form splits the
-    same items and gives the same bits; inside a capture the flag is
-    ignored and the call gives the unsplit bits."""
+    mask, the 128-key kernel and the merged correction form; with the
+    correction warpgroup, or inside a capture, the flag is ignored and the
+    call gives the unsplit bits."""
     B, H, S = 4, 16, 2048
     assert _tail(B, H, S, S) == _tail(B, H, S, S, flags=fa.FA_FLAG_TAIL_SPLIT) > 0
     assert _tail(B, H, S, S, flags=PAIR) == 0
     assert fa.fa_prefill_tail_items(B, H, S, S, 128, True, torch.bfloat16, SPLIT) == 0
     assert _tail(B, H, S, S, flags=SPLIT | fa.FA_FLAG_PAIR64) == 0
     assert _tail(B, H, S, S, flags=SPLIT | fa.FA_FLAG_SINGLE_CTA) == 0
+    assert _tail(B, H, S, S, flags=SPLIT | fa.FA_FLAG_CORRECTION_WG) == 0
     q, k, v = (t.cuda() for t in inputs.make_qkv(B, H, S, S, 128, "bf16", 66))
     o0, l0 = fa.fa_fwd(q, k, v)
     o1, l1 = fa.fa_fwd_ex(q, k, v, flags=fa.FA_FLAG_TAIL_SPLIT)
     o2, l2 = fa.fa_fwd_ex(q, k, v, flags=fa.FA_FLAG_TAIL_SPLIT | fa.FA_FLAG_CORRECTION_WG)
     torch.cuda.synchronize()
-    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert torch.equal(o0, o2) and torch.equal(l0, l2)
     assert not torch.equal(o0, o1)
+    _assert(check(q.cpu(), k.cpu(), v.cpu(), o1, l1, False, "bf16",
+                  rows=np.arange(60 * S, 64 * S, 5)))
     o, lse = torch.empty_like(o0), torch.empty_like(l0)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
