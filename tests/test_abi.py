@@ -40,6 +40,22 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, n), f"{n} declared in fa.h but not exported"
 
 
+def test_binding_constants_match_the_header():
+    """Every FA_FLAG_*, status and dtype constant of include/fa.h has the
+    same value in the Python binding, and the binding names no flag the
+    header lacks."""
+    from attention_forward_gb300 import fa
+    text = open(HEADER).read()
+    flags = {n: int(v, 16) for n, v in re.findall(r"#define (FA_FLAG_\w+) (0x[0-9a-fA-F]+)u", text)}
+    assert len(flags) >= 10
+    for n, v in flags.items():
+        assert getattr(fa, n) == v, n
+    assert {n for n in dir(fa) if n.startswith("FA_FLAG_")} == set(flags)
+    assert len(set(flags.values())) == len(flags)  # no two flags share a bit
+    for n, v in re.findall(r"\b(FA_(?:OK|ERR_\w+|F16|BF16))\s*=\s*(\d+)", text):
+        assert getattr(fa, n) == int(v), n
+
+
 def test_status_strings_and_version(lib):
     from attention_forward_gb300 import fa
     for st in range(6):
